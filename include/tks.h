@@ -1,0 +1,145 @@
+/*
+ * tks.h - C ABI of libtks, a GB300 (sm_103a) top-k index selector for
+ * DeepSeek-Sparse-Attention-style indexer logits.
+ *
+ * The operation ("Technical Deep Dive | How to Use FlagOS's New Triton-TLE
+ * Language to Build a TopK Selector Faster Than FlashInfer", section
+ * "01. Why the TopK Selector Needs Optimization", step 2 of the three-step
+ * workflow): for every row of logits, return the positions of the k largest
+ * values; indices only, no sorted output.  It is computed by radix selection
+ * (same page, section "02. Traditional GPU Approach: Radix Selection"):
+ * logits are mapped to order-preserving unsigned keys, keys are binned by
+ * digits from the most significant bits down, a histogram of each digit
+ * locates the bin holding the k-th element, the rest are discarded, and the
+ * elements above the final threshold are collected.
+ *
+ * Result order and ties.  Positions are ranked by value, largest first; +0.0
+ * ranks above -0.0; equal values rank by position, lowest first (the page's
+ * collection step appends equal values in scan order).  -inf is an ordinary
+ * (lowest) value.  Subnormals keep their exact order.  NaN inside a row's
+ * valid length is outside the contract (no error is raised; the result is
+ * unspecified).  The selected set is unique; its order within the output row
+ * is unspecified.
+ *
+ * Everything here is plain C: pointers, sizes and a CUDA stream passed as
+ * void* (a cudaStream_t; NULL is the legacy default stream).
+ */
+#ifndef TKS_H
+#define TKS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logit element types. */
+typedef enum {
+    TKS_F32 = 0,  /* IEEE binary32 */
+    TKS_BF16 = 1  /* bfloat16, stored as its 16 raw bits */
+} tks_dtype;
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    TKS_OK = 0,
+    TKS_E_INVAL = 1,       /* a bad argument; nothing was launched */
+    TKS_E_UNSUPPORTED = 2, /* no usable device (not sm_100-class or no CUDA device) */
+    TKS_E_CUDA = 3,        /* a CUDA runtime call failed (allocation, launch) */
+    TKS_E_TIMEOUT = 4,     /* a device-side wait between thread blocks gave up */
+    TKS_E_INTERNAL = 5,    /* a device-side consistency check failed */
+    TKS_E_ROW_LEN = 6      /* a device row length was < 0 or > row_stride (clamped) */
+} tks_status;
+
+/* Largest k accepted. */
+#define TKS_K_MAX (1 << 24)
+
+/*
+ * tks_topk_indices - enqueue the top-k selection of `batch` rows on `stream`.
+ *
+ *   logits      device pointer, `batch` rows of `row_stride` elements of type
+ *               `dtype`, row r starting at element r * row_stride.  Must be
+ *               aligned to the element size.  Only the first row_len[r]
+ *               elements of row r are read, each exactly once from HBM.
+ *   row_len     device pointer to `batch` int32 valid lengths, or NULL (every
+ *               row has row_stride valid elements).  A length outside
+ *               [0, row_stride] is clamped into it and reported as
+ *               TKS_E_ROW_LEN by tks_device_status().
+ *   batch       number of rows, >= 0 (0 enqueues nothing).
+ *   row_stride  elements between row starts, 0 <= row_stride < 2^31.
+ *   k           number of positions to select per row, 1 <= k <= TKS_K_MAX.
+ *   dtype       a tks_dtype.
+ *   out_idx     device pointer, int32 [batch][k] with row stride k.  Slots
+ *               0 .. min(k, len)-1 of row r receive the selected positions
+ *               (0-based within the row) in unspecified order; slots
+ *               min(k, len) .. k-1 receive -1.
+ *   stream      a cudaStream_t (NULL: the legacy default stream).
+ *
+ * Ownership: the caller owns logits, row_len and out_idx, which must stay
+ * valid until the enqueued work completes; the library keeps no reference to
+ * them.  The library owns a per-(device, stream) workspace, allocated and
+ * zeroed on the first call made on that stream (so make that first call
+ * before any CUDA-graph capture on the stream); later calls allocate nothing
+ * and never synchronise, so they can be captured.  Calls on one stream run in
+ * order; calls on different streams use different workspaces.
+ *
+ * Errors: argument errors return TKS_E_INVAL and launch nothing; CUDA errors
+ * during setup or launch return TKS_E_CUDA.  Errors detected on the device
+ * are recorded in the stream's workspace; read them with tks_device_status().
+ * Returns TKS_OK once the work is enqueued.
+ */
+int tks_topk_indices(const void *logits, const int32_t *row_len, int32_t batch,
+                     int64_t row_stride, int32_t k, int32_t dtype, int32_t *out_idx,
+                     void *stream);
+
+/*
+ * tks_device_status - synchronise `stream`, then return and clear the first
+ * device-side error recorded by calls on it (TKS_OK if none, or if no call
+ * was ever made on it).  After an error the stream's workspace is re-zeroed,
+ * so the next call starts clean.  Returns TKS_E_CUDA if synchronising fails.
+ */
+int tks_device_status(void *stream);
+
+/* A static English description of a status code (never NULL). */
+const char *tks_status_string(int status);
+
+/* Version of the library as major * 10000 + minor * 100 + patch. */
+int tks_version(void);
+
+/* Frees every workspace the library holds (call with no work in flight). */
+int tks_release(void);
+
+/*
+ * Tuning and test options (process-wide; take effect at the next call).
+ *   TKS_OPT_FORCE_GROUP      thread blocks per row: 0 = automatic, else the
+ *                            value, clamped to what the device can co-schedule
+ *   TKS_OPT_SPIN_LIMIT_NS    how long a block waits for the others of its row
+ *                            before giving up with TKS_E_TIMEOUT (default 1 s)
+ *   TKS_OPT_MIN_PER_BLOCK    automatic split: at least this many elements per
+ *                            block (default chosen by measurement)
+ *   TKS_OPT_TEST_SKIP_ARRIVE test only: 1 makes the first block of each row
+ *                            skip its first arrival, so the others' waits run
+ *                            out and report TKS_E_TIMEOUT; 0 = off
+ * Returns TKS_E_INVAL for an unknown option or a negative value.
+ */
+typedef enum {
+    TKS_OPT_FORCE_GROUP = 1,
+    TKS_OPT_SPIN_LIMIT_NS = 2,
+    TKS_OPT_MIN_PER_BLOCK = 3,
+    TKS_OPT_TEST_SKIP_ARRIVE = 4
+} tks_option;
+int tks_set_option(int option, int64_t value);
+
+/*
+ * tks_plan - the launch the next tks_topk_indices call with these sizes would
+ * use on the current device: thread blocks per row (`group`) and grid size.
+ * Either output pointer may be NULL.  Returns TKS_E_UNSUPPORTED without a
+ * usable device.
+ */
+int tks_plan(int32_t batch, int64_t row_stride, int32_t k, int32_t dtype, int32_t *group,
+             int32_t *grid);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TKS_H */
