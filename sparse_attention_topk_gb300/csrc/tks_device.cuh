@@ -1,6 +1,6 @@
 // Device building blocks of the top-k selector: the order-preserving key map,
-// the digit schedule, block-wide scans, histogram updates, TMA bulk copies and
-// bounded waits.  Written for sm_103a (GB300).
+// the digit schedule, block-wide scans, histogram and slot counters, bulk
+// asynchronous copies and bounded waits.  Written for sm_103a (GB300).
 #pragma once
 
 #include <cstdint>
@@ -10,19 +10,23 @@ namespace tks {
 // ---------------------------------------------------------------------------
 // Shape constants
 // ---------------------------------------------------------------------------
-constexpr int kThreads = 1024;               // one block per SM, 32 warps
+// 256 threads per block, one block per SM.  Control steps (scans, threshold
+// search, bookkeeping) are issued once per warp, so fewer warps make them
+// faster; the streaming steps are bound by data, not by the warp count.
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDigitBits = 12;            // widest digit: 4096 bins (16 KiB of counters)
 constexpr int kMaxBins = 1 << kMaxDigitBits;
 constexpr int kMaxRounds = 6;                // fp32: 3 key digits + up to 3 position digits
 constexpr int kSliceBytes = 160 * 1024;      // on-chip copy of a block's slice of the row
-constexpr int kLocalCandCap = 6144;          // (key, position) pairs kept by a lone block
+constexpr int kLocalCandCap = 4096;          // (key, position) pairs kept by a lone block
 constexpr int kGroupCandCap = kSliceBytes / 8;  // pairs the finishing block can hold
-constexpr int kChunks = 4;                   // bulk copies (and mbarriers) per slice
+constexpr int kChunks = 2;                   // bulk copies (and mbarriers) per slice
 
 // Dynamic shared memory layout.
-constexpr int kHistOff = 0;
-constexpr int kCtlOff = kHistOff + kMaxBins * 4;
+constexpr int kHistOff = 0;                          // counts, then exclusive suffix sums
+constexpr int kOffsOff = kHistOff + kMaxBins * 4;    // this block's offset inside each bin
+constexpr int kCtlOff = kOffsOff + kMaxBins * 4;
 constexpr int kCtlBytes = 1024;
 constexpr int kSliceOff = kCtlOff + kCtlBytes;
 constexpr int kLocalCandOff = kSliceOff + kSliceBytes;
@@ -33,30 +37,35 @@ constexpr unsigned kStatTimeout = 1u << 0;
 constexpr unsigned kStatRowLen = 1u << 1;
 constexpr unsigned kStatInternal = 1u << 2;
 
-// Per-row workspace for rows split over several blocks ("slot").
+// Per-row workspace for rows split over several blocks ("slot").  Calls on
+// a slot alternate between two sets of counters by the parity of `epoch`, so
+// the set a call uses was cleared during the previous call and nothing has to
+// be reset at the end of a call.
 struct SlotHdr {
-  unsigned arrive;           // barrier arrivals, monotonic within a call
-  unsigned done;             // blocks finished with the row
-  unsigned long long alloc;  // low 32 bits: output slots taken; high 32: candidates pushed
-  unsigned pad[12];
+  unsigned epoch;       // calls that used this slot so far
+  unsigned used[2];     // digit rounds the last call of each parity used
+  unsigned pad0;
+  unsigned arrive[2];   // barrier arrivals per parity, monotonic within a call
+  unsigned pad[10];
 };
 static_assert(sizeof(SlotHdr) == 64, "slot header is one 64-byte line");
 constexpr size_t kSlotHistOff = sizeof(SlotHdr);
-constexpr size_t kSlotCandOff = kSlotHistOff + size_t(kMaxRounds) * kMaxBins * 4;
-constexpr size_t kSlotBytes = (kSlotCandOff + size_t(kGroupCandCap) * 8 + 255) & ~size_t(255);
+constexpr size_t kSlotHistWords = size_t(kMaxRounds) * kMaxBins;  // per parity
+constexpr size_t kSlotBytes = (kSlotHistOff + 2 * kSlotHistWords * 4 + 255) & ~size_t(255);
+// Candidate slots: one 64-bit word (key | position << 32) each; all ones
+// means "not written yet" (a position is always below 2^31).
+constexpr size_t kCandSlotBytes = size_t(kGroupCandCap) * 8;
+constexpr unsigned long long kCandEmpty = ~0ull;
 constexpr size_t kWsHeaderBytes = 256;  // status word + padding
 
 // Shared-memory control block.
 struct Ctl {
   unsigned long long mbar[kChunks];
-  unsigned long long warp64[kWarps];
-  unsigned warp32[kWarps];
+  unsigned warp32[kWarps + 1];
   unsigned pick_bin, pick_above, pick_cnt;
   unsigned ok;
-  unsigned long long base64;
-  unsigned out_count;
-  unsigned cand_count;
-  unsigned is_last;
+  unsigned count;
+  unsigned red[4 * kWarps];
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block fits");
 
@@ -152,32 +161,12 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ unsigned ld_cg_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint2 ld_cg_u2(const uint2* p) {
-  uint2 v;
-  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void red_add_u32(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -213,127 +202,248 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned 
       : "memory");
   return ok != 0;
 }
+// The logits are read exactly once: ask L2 to evict them first, so they do
+// not push the kernel's own counters and candidates out.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes,
-                                              unsigned long long* bar) {
+                                              unsigned long long* bar, unsigned long long policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+      "[%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ unsigned long long policy_evict_first() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // ---------------------------------------------------------------------------
-// Block-wide scans (kThreads threads, all must call)
+// Block-wide scan (kThreads threads, all must call): sum of v over threads
+// with a higher index.  *total gets the sum over all threads.
 // ---------------------------------------------------------------------------
-
-// Sum of v over threads with a higher index (exclusive suffix sum).  *total gets the sum.
 __device__ __forceinline__ unsigned block_suffix_excl(unsigned v, unsigned* total, Ctl* ctl) {
-  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   unsigned x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     unsigned y = __shfl_down_sync(0xffffffffu, x, off);
     if (lane + off < 32) x += y;
   }
-  // x = sum over lanes >= lane
+  // x = sum over lanes >= lane of this warp
   if (lane == 0) ctl->warp32[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    unsigned w = ctl->warp32[lane];
+  unsigned higher = 0, all = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      unsigned y = __shfl_down_sync(0xffffffffu, w, off);
-      if (lane + off < 32) w += y;
-    }
-    ctl->warp32[lane] = w;  // sum over warps >= lane
+  for (int w = 0; w < kWarps; ++w) {
+    const unsigned s = ctl->warp32[w];
+    all += s;
+    if (w > (int)warp) higher += s;
   }
-  __syncthreads();
-  unsigned higher_warps = warp + 1 < kWarps ? ctl->warp32[warp + 1] : 0u;
-  *total = ctl->warp32[0];
-  unsigned r = (x - v) + higher_warps;
+  *total = all;
   __syncthreads();  // warp32 reusable afterwards
-  return r;
+  return (x - v) + higher;
 }
 
-// Exclusive prefix sum of a 64-bit value over threads in index order; *total gets the sum.
-__device__ __forceinline__ unsigned long long block_prefix_excl64(unsigned long long v,
-                                                                  unsigned long long* total,
-                                                                  Ctl* ctl) {
-  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long x = v;
+// ---------------------------------------------------------------------------
+// Counters updated by whole warps.
+// ---------------------------------------------------------------------------
+
+// Output slots for U elements per lane: o[j] = old value of c[d[j]] after
+// adding 1 for every selected element.  A full warp whose selected elements
+// all share lane 0's counter takes its slots with one add; otherwise the
+// selected elements add independently (no chain of votes per element).
+template <int U>
+__device__ __forceinline__ void slots_vec(unsigned* c, const uint32_t (&d)[U], unsigned sel,
+                                          unsigned (&o)[U]) {
+  constexpr unsigned kAll = (1u << U) - 1u;
+  bool uni = sel == kAll;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    unsigned long long y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= (unsigned)off) x += y;
-  }
-  if (lane == 31) ctl->warp64[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long w = ctl->warp64[lane];
+  for (int j = 1; j < U; ++j) uni &= d[j] == d[0];
+  const uint32_t d0 = __shfl_sync(0xffffffffu, d[0], 0);
+  if (__all_sync(0xffffffffu, uni && d[0] == d0)) {
+    unsigned base = 0;
+    if (lane_id() == 0) base = atomicAdd(&c[d0], 32u * U);
+    base = __shfl_sync(0xffffffffu, base, 0) + lane_id() * U;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      unsigned long long y = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= (unsigned)off) w += y;
-    }
-    ctl->warp64[lane] = w;  // inclusive over warps <= lane
-  }
-  __syncthreads();
-  unsigned long long lower = warp > 0 ? ctl->warp64[warp - 1] : 0ull;
-  *total = ctl->warp64[kWarps - 1];
-  unsigned long long r = (x - v) + lower;
-  __syncthreads();
-  return r;
-}
-
-// ---------------------------------------------------------------------------
-// Histogram update, called by all 32 lanes of a warp.  When every valid lane
-// of the warp hits the same bin (constant or plateau rows) one lane adds the
-// whole count; otherwise each valid lane adds one.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void hist_add(unsigned* h, uint32_t d, bool valid) {
-  const unsigned full = 0xffffffffu;
-  unsigned vm = __ballot_sync(full, valid);
-  if (vm == 0) return;
-  int first = __ffs(vm) - 1;
-  uint32_t d0 = __shfl_sync(full, d, first);
-  bool same = __all_sync(full, !valid || d == d0);
-  if (same) {
-    if ((int)(threadIdx.x & 31) == first) atomicAdd(&h[d0], (unsigned)__popc(vm));
-  } else if (valid) {
-    atomicAdd(&h[d], 1u);
+    for (int j = 0; j < U; ++j) o[j] = base + j;
+  } else {
+#pragma unroll
+    for (int j = 0; j < U; ++j) o[j] = ((sel >> j) & 1u) ? atomicAdd(&c[d[j]], 1u) : 0u;
   }
 }
 
-// ---------------------------------------------------------------------------
-// Threshold scan: the bin holding the k_rem-th largest element (1-based) of
-// the histogram, the count strictly above it and its own count.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void find_bin(const unsigned* h, int nb, unsigned k_rem, Ctl* ctl) {
-  const int per = (nb + kThreads - 1) / kThreads;
-  const int b0 = threadIdx.x * per;
-  unsigned s = 0;
-  for (int i = 0; i < per; ++i) {
-    int b = b0 + i;
-    if (b < nb) s += h[b];
+// Ranks for U selected-or-not elements per lane against one shared counter:
+// one add per warp call, ranks from ballots.
+template <int U>
+__device__ __forceinline__ void ranks_vec(unsigned* counter, unsigned sel, unsigned (&o)[U]) {
+  const unsigned lt = (1u << lane_id()) - 1u;
+  unsigned before = 0, mine[U];
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const unsigned m = __ballot_sync(0xffffffffu, (sel >> j) & 1u);
+    mine[j] = before + (unsigned)__popc(m & lt);
+    before += (unsigned)__popc(m);
   }
-  unsigned total;
-  unsigned above = block_suffix_excl(s, &total, ctl);
-  if (s != 0 && above < k_rem && k_rem <= above + s) {
-    unsigned acc = above;
-    for (int i = per - 1; i >= 0; --i) {
-      int b = b0 + i;
-      if (b >= nb) continue;
-      unsigned c = h[b];
-      if (k_rem <= acc + c) {
-        ctl->pick_bin = (unsigned)b;
-        ctl->pick_above = acc;
-        ctl->pick_cnt = c;
-        break;
+  unsigned base = 0;
+  if (lane_id() == 0 && before) base = atomicAdd(counter, before);
+  base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+  for (int j = 0; j < U; ++j) o[j] = base + mine[j];
+}
+
+// Histogram update for U elements per lane (one vote per call): if every
+// lane's U elements are valid and share lane 0's bin, lane 0 adds 32*U once
+// (constant and plateau rows); otherwise every valid element adds 1 with
+// independent atomics.
+template <int U>
+__device__ __forceinline__ void hist_add_vec(unsigned* h, const uint32_t (&d)[U], unsigned vm) {
+  constexpr unsigned kAll = (1u << U) - 1u;
+  bool uni = vm == kAll;
+#pragma unroll
+  for (int j = 1; j < U; ++j) uni &= d[j] == d[0];
+  const uint32_t d0 = __shfl_sync(0xffffffffu, d[0], 0);
+  if (__all_sync(0xffffffffu, uni && d[0] == d0)) {
+    if (lane_id() == 0) atomicAdd(&h[d0], 32u * U);
+  } else {
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if ((vm >> j) & 1u) atomicAdd(&h[d[j]], 1u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Threshold scan over h[0..nb): the bin holding the k_rem-th largest element
+// (1-based), the count strictly above it and its own count.  Rewrites h in
+// place into exclusive suffix sums (h[i] = number of elements in bins > i),
+// which later give every emitted element its output slot.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void note_pick(Ctl* ctl, unsigned bin, unsigned above, unsigned c,
+                                          unsigned k_rem) {
+  if (above < k_rem && k_rem <= above + c) {
+    ctl->pick_bin = bin;
+    ctl->pick_above = above;
+    ctl->pick_cnt = c;
+  }
+}
+
+__device__ __forceinline__ void pick_and_suffix(unsigned* h, int nb, unsigned k_rem, Ctl* ctl) {
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  if (nb >= kWarps * 128) {
+    // Warp w owns a contiguous run of 128*Q bins; lane l reads 16-byte vector
+    // q*32 + l of it, so every access is conflict-free.  Bin order inside the
+    // run is (q, lane, element).
+    const int Q = nb / (kWarps * 128);  // 1, 2 or 4
+    uint4* h4 = reinterpret_cast<uint4*>(h) + warp * 32 * Q;
+    uint4 v[4];
+    unsigned tot[4], sq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[q] = q < Q ? h4[q * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+      const unsigned t = v[q].x + v[q].y + v[q].z + v[q].w;
+      unsigned x = t;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32) x += y;
       }
-      acc += c;
+      sq[q] = x - t;                                 // lanes above, same q
+      tot[q] = __shfl_sync(0xffffffffu, x, 0);       // all lanes, same q
     }
+    unsigned above_q[4], acc = 0;
+#pragma unroll
+    for (int q = 3; q >= 0; --q) {
+      above_q[q] = acc;
+      acc += tot[q];
+    }
+    if (lane == 0) ctl->warp32[warp] = acc;
+    __syncthreads();
+    unsigned higher = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      if (w > (int)warp) higher += ctl->warp32[w];
+    const unsigned base_bin = warp * 128 * Q + lane * 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q >= Q) continue;
+      unsigned a = higher + above_q[q] + sq[q];
+      const unsigned bq = base_bin + q * 128;
+      uint4 o;
+      o.w = a; note_pick(ctl, bq + 3, a, v[q].w, k_rem); a += v[q].w;
+      o.z = a; note_pick(ctl, bq + 2, a, v[q].z, k_rem); a += v[q].z;
+      o.y = a; note_pick(ctl, bq + 1, a, v[q].y, k_rem); a += v[q].y;
+      o.x = a; note_pick(ctl, bq + 0, a, v[q].x, k_rem);
+      h4[q * 32 + lane] = o;
+    }
+    __syncthreads();
+    return;
+  }
+  // Small digits: thread t owns `per` consecutive bins.
+  const int per = (nb + kThreads - 1) / kThreads;  // 1..3
+  const int b0 = threadIdx.x * per;
+  unsigned c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (i < per && b0 + i < nb) ? h[b0 + i] : 0u;
+  const unsigned s = c[0] + c[1] + c[2] + c[3];
+  unsigned total;
+  unsigned acc = block_suffix_excl(s, &total, ctl);
+#pragma unroll
+  for (int i = 3; i >= 0; --i) {
+    if (i < per && b0 + i < nb) {
+      note_pick(ctl, (unsigned)(b0 + i), acc, c[i], k_rem);
+      h[b0 + i] = acc;
+    }
+    acc += c[i];
   }
   __syncthreads();
+}
+
+// Block-wide OR and AND of per-thread partial results for two words
+// (all threads call; every thread gets the totals).
+__device__ __forceinline__ void block_or_and(uint32_t& or_a, uint32_t& and_a, uint32_t& or_b,
+                                             uint32_t& and_b, Ctl* ctl) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    or_a |= __shfl_xor_sync(0xffffffffu, or_a, off);
+    and_a &= __shfl_xor_sync(0xffffffffu, and_a, off);
+    or_b |= __shfl_xor_sync(0xffffffffu, or_b, off);
+    and_b &= __shfl_xor_sync(0xffffffffu, and_b, off);
+  }
+  const unsigned warp = threadIdx.x >> 5;
+  if (lane_id() == 0) {
+    ctl->red[4 * warp + 0] = or_a;
+    ctl->red[4 * warp + 1] = and_a;
+    ctl->red[4 * warp + 2] = or_b;
+    ctl->red[4 * warp + 3] = and_b;
+  }
+  __syncthreads();
+  or_a = 0u; and_a = ~0u; or_b = 0u; and_b = ~0u;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    or_a |= ctl->red[4 * w + 0];
+    and_a &= ctl->red[4 * w + 1];
+    or_b |= ctl->red[4 * w + 2];
+    and_b &= ctl->red[4 * w + 3];
+  }
+  __syncthreads();
+}
+
+// Candidate words in global memory, written and polled without caching.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 }  // namespace tks

@@ -11,14 +11,17 @@
 // walk simply continues into the position bits when values tie.
 //
 // Layout of the work (one kernel launch per call):
-//  * A row is split into `group` contiguous slices, one thread block (1024
+//  * A row is split into `group` contiguous slices, one thread block (256
 //    threads, one per SM) each.  Each block copies its slice from HBM once,
 //    with bulk asynchronous copies (TMA, non-tensor form) into shared memory,
 //    and builds a 4096-bin histogram of the top 12 key bits on chip.
 //  * With group > 1 the blocks of a row add their histograms into one in L2
 //    and meet at a bounded barrier; every block then finds the threshold bin
 //    itself (the page's "TLE distributed" idea of summing block histograms
-//    and continuing with the new threshold, section "5. Triton-TLE").
+//    and continuing with the new threshold, section "5. Triton-TLE").  The
+//    adds return each block's offset inside every bin, so each block can
+//    later write its selected positions to fixed output slots with no
+//    further coordination.
 //  * As soon as the bin holding the k-th element has few enough members
 //    (the page's "early stop when the bucket is small", section "03."),
 //    blocks write every position above the bin to the output and push the
@@ -52,6 +55,7 @@ struct Params {
   int32_t group;
   int32_t test_skip_arrive;
   unsigned char* ws;
+  int32_t slots;
   long long spin_limit_ns;
 };
 
@@ -101,59 +105,81 @@ struct Slice {
 };
 
 // ---------------------------------------------------------------------------
-// Element sources.  visit(f) calls f(key, position, valid) with all 32 lanes
-// of each warp together (f may use warp intrinsics); the order in which a
-// thread meets its elements is the same on every visit.
+// Element sources.  visit(f) hands each lane U elements at a time:
+// f(key[U], pos[U], vm), bit j of vm set when element j is real.  All 32
+// lanes of a warp call f together (f may vote once per call), and a thread
+// meets its elements in the same order on every visit.
 // ---------------------------------------------------------------------------
 template <int DT>
 struct SliceSrc {
+  static constexpr int U = Elt<DT>::V;
   const unsigned char* row;  // the row in global memory
   const unsigned char* sm;   // on-chip copy (resident slices)
   Slice s;
 
   template <class F>
-  __device__ __forceinline__ void visit_vecs(int va, int vb, F&& f) const {
+  __device__ __forceinline__ void vec(const uint4& x, int i0, unsigned vm, F& f) const {
     using E = Elt<DT>;
+    uint32_t key[U];
+    int pos[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      key[j] = E::key(E::lane(x, j));
+      pos[j] = i0 + j;
+    }
+    f(key, pos, vm);
+  }
+
+  // 16-byte vectors [va, vb) of the on-chip copy.
+  template <class F>
+  __device__ __forceinline__ void visit_vecs(int va, int vb, F&& f) const {
     for (int v0 = va; v0 < vb; v0 += kThreads) {
       const int v = v0 + (int)threadIdx.x;
-      const bool in = v < vb;
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (in) x = reinterpret_cast<const uint4*>(sm)[v];
-      const int i0 = s.o + v * E::V;
-#pragma unroll
-      for (int j = 0; j < E::V; ++j) {
-        const int i = i0 + j;
-        f(E::key(E::lane(x, j)), i, in && i >= s.lo && i < s.hi);
+      unsigned vm = 0u;
+      if (v < vb) {
+        x = reinterpret_cast<const uint4*>(sm)[v];
+        const int i0 = s.o + v * U;
+        vm = (1u << U) - 1u;
+        if (i0 < s.lo) vm &= ~0u << (s.lo - i0);
+        if (i0 + U > s.hi) vm &= (1u << max(0, s.hi - i0)) - 1u;
       }
+      vec(x, s.o + v * U, vm, f);
     }
   }
 
+  // Straight from global memory (slices too large to keep on chip).
   template <class F>
   __device__ __forceinline__ void visit_global(F&& f) const {
     using E = Elt<DT>;
     const int nh = s.bl - s.lo, nt = s.hi - s.bh;
-    if ((threadIdx.x >> 5) == 0) {
+    if ((threadIdx.x >> 5) == 0) {  // the unaligned head and tail, one element per lane
       const int l = threadIdx.x & 31;
       const bool v = l < nh + nt;
       const int i = l < nh ? s.lo + l : s.bh + (l - nh);
-      const uint32_t raw = v ? E::load(row, i) : 0u;
-      f(E::key(raw), i, v);
+      uint32_t key[U];
+      int pos[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        key[j] = E::key(v && j == 0 ? E::load(row, i) : 0u);
+        pos[j] = i;
+      }
+      f(key, pos, v ? 1u : 0u);
     }
     const uint4* body = reinterpret_cast<const uint4*>(row + (int64_t)s.bl * E::ES);
-    const int nv = (s.bh - s.bl) / E::V;
-    constexpr int U = 4;
-    for (int v0 = 0; v0 < nv; v0 += U * kThreads) {
-      uint4 x[U];
+    const int nv = (s.bh - s.bl) / U;
+    constexpr int kAhead = 4;
+    for (int v0 = 0; v0 < nv; v0 += kAhead * kThreads) {
+      uint4 x[kAhead];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * kThreads + (int)threadIdx.x;
-        x[u] = v < nv ? ld_nc_v4(body + v) : make_uint4(0u, 0u, 0u, 0u);
+      for (int a = 0; a < kAhead; ++a) {
+        const int v = v0 + a * kThreads + (int)threadIdx.x;
+        x[a] = v < nv ? ld_nc_v4(body + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * kThreads + (int)threadIdx.x;
-#pragma unroll
-        for (int j = 0; j < E::V; ++j) f(E::key(E::lane(x[u], j)), s.bl + v * E::V + j, v < nv);
+      for (int a = 0; a < kAhead; ++a) {
+        const int v = v0 + a * kThreads + (int)threadIdx.x;
+        vec(x[a], s.bl + v * U, v < nv ? (1u << U) - 1u : 0u, f);
       }
     }
   }
@@ -167,17 +193,29 @@ struct SliceSrc {
   }
 };
 
-// (key, position) pairs in shared memory.
+// (key, position) pairs in shared memory, four per lane per call.
 struct CandSrc {
+  static constexpr int U = 4;
   const uint2* c;
   unsigned n;
   template <class F>
   __device__ __forceinline__ void visit(F&& f) const {
-    for (unsigned i0 = 0; i0 < n; i0 += kThreads) {
-      const unsigned i = i0 + threadIdx.x;
-      const bool v = i < n;
-      const uint2 e = v ? c[i] : make_uint2(0u, 0u);
-      f(e.x, (int)e.y, v);
+    for (unsigned i0 = 0; i0 < n; i0 += U * kThreads) {
+      uint32_t key[U];
+      int pos[U];
+      unsigned vm = 0u;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const unsigned i = i0 + j * kThreads + threadIdx.x;
+        uint2 e = make_uint2(0u, 0u);
+        if (i < n) {
+          e = c[i];
+          vm |= 1u << j;
+        }
+        key[j] = e.x;
+        pos[j] = (int)e.y;
+      }
+      f(key, pos, vm);
     }
   }
 };
@@ -186,18 +224,27 @@ struct CandSrc {
 // Block-level steps
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void zero_hist(unsigned* h, int nb) {
-  for (int i = threadIdx.x; i < nb; i += kThreads) h[i] = 0u;
+// Zeroes counters [0, n) (n rounded up to a multiple of 4; arrays hold kMaxBins).
+__device__ __forceinline__ void zero_counters(unsigned* h, int n) {
+  uint4* h4 = reinterpret_cast<uint4*>(h);
+  for (int i = threadIdx.x; i < (n + 3) / 4; i += kThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Histogram of digit D over the elements that match the prefix.
 template <class Src>
 __device__ __forceinline__ void hist_round(const Src& src, unsigned* h, const Prefix& P, Digit D,
                                            uint32_t pmax) {
-  src.visit([&](uint32_t key, int pos, bool valid) {
-    const uint32_t inv = pmax - (uint32_t)pos;
-    const bool m = valid && prefix_cmp(P, key, inv) == 0;
-    hist_add(h, digit_value(D, key, inv), m);
+  constexpr int U = Src::U;
+  src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+    uint32_t d[U];
+    unsigned m = 0u;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t inv = pmax - (uint32_t)pos[j];
+      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0) m |= 1u << j;
+      d[j] = digit_value(D, key[j], inv);
+    }
+    if (__any_sync(0xffffffffu, m != 0u)) hist_add_vec<U>(h, d, m);
   });
 }
 
@@ -216,22 +263,36 @@ __device__ __forceinline__ void mbar_wait_bounded(unsigned long long* bar, unsig
   }
 }
 
-// Adds this block's histogram into the row's L2 histogram, waits (bounded)
-// until every block of the row has done the same, then loads the sum.
-__device__ bool group_merge(unsigned* h, int nb, unsigned* g, SlotHdr* slot, unsigned target,
-                            bool skip_arrive, long long limit, Ctl* ctl, unsigned* status) {
-  for (int i = threadIdx.x; i < nb; i += kThreads) {
-    const unsigned c = h[i];
-    if (c) red_add_u32(&g[i], c);
+// Adds this block's counts into the row's L2 histogram.  The value each add
+// returns is this block's offset inside that bin across the row, kept in
+// offs[] to place the block's elements in the output later without any
+// further coordination.  Then a bounded barrier over the row's blocks, then
+// the row's summed counts replace the local ones in h[].
+__device__ bool group_merge(unsigned* h, unsigned* offs, int nb, unsigned* g, unsigned* arrive,
+                            unsigned target, bool skip_arrive, long long limit, Ctl* ctl,
+                            unsigned* status) {
+  constexpr int kPer = kMaxBins / kThreads;
+  unsigned c[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    c[j] = b < nb ? h[b] : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    if (b < nb) offs[b] = c[j];
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    if (!skip_arrive) atomicAdd(&slot->arrive, 1u);
+    if (!skip_arrive) atomicAdd(arrive, 1u);
     unsigned ok = 1u;
-    if (ld_acquire_u32(&slot->arrive) < target) {
+    if (ld_acquire_u32(arrive) < target) {
       const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_u32(&slot->arrive) < target) {
+      while (ld_acquire_u32(arrive) < target) {
         if ((long long)(globaltimer_ns() - t0) > limit) {
           ok = 0u;
           atomicOr(status, kStatTimeout);
@@ -244,81 +305,28 @@ __device__ bool group_merge(unsigned* h, int nb, unsigned* g, SlotHdr* slot, uns
   }
   __syncthreads();
   if (!ctl->ok) return false;
-  for (int i = threadIdx.x; i < nb; i += kThreads) h[i] = ld_cg_u32(&g[i]);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    c[j] = b < nb ? __ldcg(g + b) : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    if (b < nb) h[b] = c[j];
+  }
   __syncthreads();
   return true;
 }
 
-// Output slots and candidate slots come from one 64-bit counter: low half
-// output positions, high half candidates.
-struct Reserve {
-  unsigned long long* global;  // slot->alloc (rows split over blocks), else null
-};
-
-// Writes every element whose resolved prefix is above P (and, unless
-// `collect`, equal to P) to the output row; with `collect` the elements equal
-// to P go to `cand` as (key, position) pairs.  Two passes over the source:
-// count, one reservation per block, then write.
-template <class Src>
-__device__ void emit(const Src& src, const Prefix& P, uint32_t pmax, bool collect, Reserve res,
-                     int32_t* out_row, unsigned k, uint2* cand, unsigned cap, Ctl* ctl,
-                     unsigned* status) {
-  unsigned ne = 0, nc = 0;
-  src.visit([&](uint32_t key, int pos, bool valid) {
-    if (!valid) return;
-    const int c = prefix_cmp(P, key, pmax - (uint32_t)pos);
-    if (c > 0 || (c == 0 && !collect))
-      ++ne;
-    else if (c == 0)
-      ++nc;
-  });
-  unsigned long long total;
-  const unsigned long long mine =
-      block_prefix_excl64(((unsigned long long)nc << 32) | ne, &total, ctl);
-  if (threadIdx.x == 0) {
-    unsigned long long base;
-    if (res.global) {
-      base = total ? atomicAdd(res.global, total) : 0ull;
-    } else {
-      base = ((unsigned long long)ctl->cand_count << 32) | ctl->out_count;
-      ctl->out_count += (unsigned)total;
-      ctl->cand_count += (unsigned)(total >> 32);
-    }
-    ctl->base64 = base;
-  }
-  __syncthreads();
-  const unsigned long long base = ctl->base64;
-  unsigned eo = (unsigned)base + (unsigned)mine;
-  unsigned co = (unsigned)(base >> 32) + (unsigned)(mine >> 32);
-  bool bad = false;
-  src.visit([&](uint32_t key, int pos, bool valid) {
-    if (!valid) return;
-    const int c = prefix_cmp(P, key, pmax - (uint32_t)pos);
-    if (c > 0 || (c == 0 && !collect)) {
-      if (eo < k)
-        out_row[eo] = pos;
-      else
-        bad = true;
-      ++eo;
-    } else if (c == 0) {
-      if (co < cap)
-        cand[co] = make_uint2(key, (uint32_t)pos);
-      else
-        bad = true;
-      ++co;
-    }
-  });
-  if (bad) atomicOr(status, kStatInternal);
-  __syncthreads();
-}
-
-// Finds the threshold bin for round D; false (and an error) if the counts
-// are inconsistent, which cannot happen unless memory was corrupted.
-__device__ __forceinline__ bool pick_bin(const unsigned* h, int nb, unsigned k_rem, Ctl* ctl,
+// Finds the threshold bin of h[0..nb) and turns h into exclusive suffix sums;
+// false (and an error) if the counts are inconsistent, which cannot happen
+// unless memory was corrupted.
+__device__ __forceinline__ bool pick_bin(unsigned* h, int nb, unsigned k_rem, Ctl* ctl,
                                          unsigned* status, unsigned* bin, unsigned* above,
                                          unsigned* cnt) {
   if (threadIdx.x == 0) ctl->pick_bin = 0xFFFFFFFFu;
-  find_bin(h, nb, k_rem, ctl);
+  pick_and_suffix(h, nb, k_rem, ctl);
   *bin = ctl->pick_bin;
   *above = ctl->pick_above;
   *cnt = ctl->pick_cnt;
@@ -329,22 +337,112 @@ __device__ __forceinline__ bool pick_bin(const unsigned* h, int nb, unsigned k_r
   return true;
 }
 
+// What happens to the elements of the threshold round's bins.
+enum RoundEnd {
+  kEndFinal = 0,    // the threshold bin is taken whole: emit bins >= bin
+  kEndCollect = 1,  // emit bins > bin, bin's elements become candidates
+  kEndAbove = 2     // emit bins > bin, another digit round follows
+};
+
+// Stores a candidate (key, position) as one 64-bit word.  Global slots are
+// polled by the finishing block, so they are written with a single relaxed
+// store that is never torn.
+__device__ __forceinline__ void put_cand(uint2* cand, unsigned i, uint32_t key, int pos,
+                                         bool global) {
+  const unsigned long long w = (unsigned long long)key | ((unsigned long long)(uint32_t)pos << 32);
+  if (global)
+    st_relaxed_u64(reinterpret_cast<unsigned long long*>(cand) + i, w);
+  else
+    reinterpret_cast<unsigned long long*>(cand)[i] = w;
+}
+
+// One pass over the source: every element that matches the prefix before
+// this round and lands in an emitted bin goes to output slot
+//   base + (elements of the row in higher bins) + (its rank inside its bin),
+// the rank coming from this block's running offset offs[bin]; candidates go
+// to cand[offs[bin]++].
+template <class Src>
+__device__ void emit_round(const Src& src, const Prefix& P, Digit D, unsigned bin, int end,
+                           unsigned base, const unsigned* suf, unsigned* offs, uint32_t pmax,
+                           int32_t* out_row, unsigned k, uint2* cand, bool cand_global,
+                           unsigned cap, unsigned* status) {
+  constexpr int U = Src::U;
+  bool bad = false;
+  src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+    uint32_t d[U];
+    unsigned sel = 0u, to_cand = 0u;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t inv = pmax - (uint32_t)pos[j];
+      d[j] = digit_value(D, key[j], inv);
+      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0) {
+        if (d[j] > bin || (end == kEndFinal && d[j] == bin)) sel |= 1u << j;
+        if (end == kEndCollect && d[j] == bin) to_cand |= 1u << j;
+      }
+    }
+    sel |= to_cand;
+    if (!__any_sync(0xffffffffu, sel != 0u)) return;
+    unsigned o[U];
+    slots_vec<U>(offs, d, sel, o);
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      if (!((sel >> j) & 1u)) continue;
+      if ((to_cand >> j) & 1u) {
+        if (o[j] < cap)
+          put_cand(cand, o[j], key[j], pos[j], cand_global);
+        else
+          bad = true;
+      } else {
+        const unsigned slot = base + suf[d[j]] + o[j];
+        if (slot < k)
+          out_row[slot] = pos[j];
+        else
+          bad = true;
+      }
+    }
+  });
+  if (bad) atomicOr(status, kStatInternal);
+}
+
+// The highest still-varying bits (at most 12) of the composite key: value
+// key first, then the inverted position.  False when nothing varies.
+__device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, Digit* D) {
+  uint32_t& v = vk ? vk : vp;
+  if (!v) return false;
+  const int hi = 31 - __clz((int)v);
+  const int lo = hi >= 11 ? hi - 11 : 0;
+  *D = {vk ? 0 : 1, lo, hi - lo + 1};
+  v &= ~(((1u << (hi - lo + 1)) - 1u) << lo);
+  return true;
+}
+
 // Refines candidates held on chip until the k_rem wanted among them are
-// known, then writes them.  Rounds continue at digit t.
-template <int DT>
-__device__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Prefix P, int t,
-                               int pos_bits, uint32_t pmax, unsigned* h, int32_t* out_row,
-                               unsigned k, Ctl* ctl, unsigned* status) {
+// known, then writes them after the k - k_rem already emitted.  Bits that are
+// equal in every candidate join the prefix at once; digits are taken from the
+// highest bits that still differ, so no round is spent on a constant digit.
+// (or_*, and_*: OR and AND of the candidates' keys and inverted positions.)
+__device__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Prefix P,
+                               uint32_t or_k, uint32_t and_k, uint32_t or_i, uint32_t and_i,
+                               uint32_t pmax, unsigned* h, int32_t* out_row, unsigned k, Ctl* ctl,
+                               unsigned* status) {
   const CandSrc src{cand, n};
-  const int nr = num_rounds<DT>(pos_bits);
+  constexpr int U = CandSrc::U;
+  const unsigned out_base = k - k_rem;
+  uint32_t vk = (or_k ^ and_k) & ~P.kmask;
+  uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
+  const uint32_t ck = ~(or_k ^ and_k) & ~P.kmask, cp = ~(or_i ^ and_i) & pmax & ~P.pmask;
+  P.kmask |= ck;
+  P.kpref |= and_k & ck;
+  P.pmask |= cp;
+  P.ppref |= and_i & cp;
   for (;;) {
-    if (t >= nr) {
+    Digit D;
+    if (!next_digit(vk, vp, &D)) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
-    const Digit D = digit_of_round<DT>(t, pos_bits);
     const int nb = 1 << D.bits;
-    zero_hist(h, nb);
+    zero_counters(h, nb);
     __syncthreads();
     hist_round(src, h, P, D, pmax);
     __syncthreads();
@@ -353,9 +451,29 @@ __device__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Pr
     prefix_extend(P, D, bin);
     k_rem -= above;
     if (cnt == k_rem) break;
-    ++t;
   }
-  emit(src, P, pmax, false, Reserve{nullptr}, out_row, k, nullptr, 0u, ctl, status);
+  if (threadIdx.x == 0) ctl->count = 0u;
+  __syncthreads();
+  bool bad = false;
+  src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+    unsigned sel = 0u;
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], pmax - (uint32_t)pos[j]) >= 0) sel |= 1u << j;
+    if (!__any_sync(0xffffffffu, sel != 0u)) return;
+    unsigned o[U];
+    ranks_vec<U>(&ctl->count, sel, o);
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      if (!((sel >> j) & 1u)) continue;
+      const unsigned slot = out_base + o[j];
+      if (slot < k)
+        out_row[slot] = pos[j];
+      else
+        bad = true;
+    }
+  });
+  if (bad) atomicOr(status, kStatInternal);
 }
 
 // Selects the top k of row r with this block as part `part` of `group`.
@@ -366,6 +484,7 @@ __device__ bool select_row(const Params& p, int r, int part, unsigned char* smem
   using E = Elt<DT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   unsigned* h = reinterpret_cast<unsigned*>(smem + kHistOff);
+  unsigned* offs = reinterpret_cast<unsigned*>(smem + kOffsOff);
   unsigned char* sl = smem + kSliceOff;
   uint2* lcand = reinterpret_cast<uint2*>(smem + kLocalCandOff);
   unsigned* status = reinterpret_cast<unsigned*>(p.ws);
@@ -373,73 +492,76 @@ __device__ bool select_row(const Params& p, int r, int part, unsigned char* smem
   const unsigned k = (unsigned)p.k;
   int32_t* out_row = p.out + (int64_t)r * p.k;
 
-  __syncthreads();  // the previous row is done with ctl
-  if (threadIdx.x == 0) {
-    ctl->ok = 1u;
-    ctl->out_count = 0u;
-    ctl->cand_count = 0u;
+  __syncthreads();  // the previous row is done with shared memory
+  if (threadIdx.x == 0) ctl->ok = 1u;
+
+  // This row's slot (rows split over blocks): its header is read now and
+  // used at the first merge.
+  SlotHdr* slot = nullptr;
+  uint4 hdr = make_uint4(0u, 0u, 0u, 0u);
+  if (group > 1) {
+    slot = reinterpret_cast<SlotHdr*>(p.ws + kWsHeaderBytes + (size_t)(blockIdx.x / group) * kSlotBytes);
+    hdr = ld_relaxed_v4(slot);  // epoch, used[0], used[1]
   }
 
   // Valid length (clamped; a bad one is reported).
   int64_t Lr = p.row_len ? (int64_t)__ldg(p.row_len + r) : p.row_stride;
+  zero_counters(h, kMaxBins);
   if (Lr < 0 || Lr > p.row_stride) {
     if (threadIdx.x == 0 && part == 0) atomicOr(status, kStatRowLen);
     Lr = Lr < 0 ? 0 : p.row_stride;
   }
-  const int L = (int)Lr;
+  const uint32_t L = (uint32_t)Lr;
 
   // Rows with no more than k elements: every position, then -1.
-  if ((unsigned)L <= k) {
-    for (int64_t i = (int64_t)part * kThreads + threadIdx.x; i < (int64_t)k;
-         i += (int64_t)kThreads * group)
+  if (L <= k) {
+    for (uint32_t i = (uint32_t)part * kThreads + threadIdx.x; i < k; i += (uint32_t)kThreads * group)
       out_row[i] = i < L ? (int32_t)i : -1;
     return true;
   }
 
-  const int pos_bits = 32 - __clz(L - 1);  // 1..31
-  const uint32_t pmax = (pos_bits == 32) ? 0xFFFFFFFFu : ((1u << pos_bits) - 1u);
+  const int pos_bits = 32 - __clz((int)(L - 1u));  // 1..31
+  const uint32_t pmax = (1u << pos_bits) - 1u;
   const int nr = num_rounds<DT>(pos_bits);
 
   // This block's slice, with 16-byte aligned interior boundaries.
   const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
-  const int mis = (int)(((uintptr_t)row & 15u) / E::ES);
-  auto align_up = [&](int64_t i) -> int64_t { return i + (E::V - (mis + i) % E::V) % E::V; };
-  auto align_down = [&](int64_t i) -> int64_t { return i - (mis + i) % E::V; };
-  const int64_t chunk = (((int64_t)L + group - 1) / group + E::V - 1) / E::V * E::V;
+  const uint32_t V = E::V;
+  const uint32_t mis = (uint32_t)(((uintptr_t)row & 15u) / E::ES);
+  auto align_up = [&](uint32_t i) -> uint32_t { return i + ((V - ((mis + i) & (V - 1u))) & (V - 1u)); };
+  auto align_down = [&](uint32_t i) -> uint32_t { return i - ((mis + i) & (V - 1u)); };
+  const uint32_t chunk = ((L + (uint32_t)group - 1u) / (uint32_t)group + V - 1u) & ~(V - 1u);
   Slice s;
-  s.lo = part == 0 ? 0 : (int)min((int64_t)L, align_up((int64_t)part * chunk));
-  s.hi = part == group - 1 ? L : (int)min((int64_t)L, align_up((int64_t)(part + 1) * chunk));
-  s.bl = (int)min((int64_t)s.hi, align_up(s.lo));
-  s.bh = (int)max((int64_t)s.bl, align_down(s.hi));
-  s.o = s.lo < s.bl ? s.bl - E::V : s.bl;
-  s.nvec = (s.hi - s.o + E::V - 1) / E::V;
-  s.resident = (int64_t)s.nvec * 16 <= kSliceBytes;
+  s.lo = part == 0 ? 0 : (int)min(L, align_up((uint32_t)part * chunk));
+  s.hi = part == group - 1 ? (int)L : (int)min(L, align_up((uint32_t)(part + 1) * chunk));
+  s.bl = (int)min((uint32_t)s.hi, align_up((uint32_t)s.lo));
+  s.bh = max(s.bl, (int)align_down((uint32_t)s.hi));
+  s.o = s.lo < s.bl ? s.bl - (int)V : s.bl;
+  s.nvec = (s.hi - s.o + (int)V - 1) / (int)V;
+  s.resident = s.nvec * 16 <= kSliceBytes;
   const SliceSrc<DT> src{row, sl, s};
 
-  SlotHdr* slot = nullptr;
-  unsigned* slot_hist = nullptr;
-  uint2* slot_cand = nullptr;
-  if (group > 1) {
-    unsigned char* base = p.ws + kWsHeaderBytes + (size_t)(blockIdx.x / group) * kSlotBytes;
-    slot = reinterpret_cast<SlotHdr*>(base);
-    slot_hist = reinterpret_cast<unsigned*>(base + kSlotHistOff);
-    slot_cand = reinterpret_cast<uint2*>(base + kSlotCandOff);
-  }
-
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
-  zero_hist(h, kMaxBins);
+  constexpr int U = SliceSrc<DT>::U;
+  auto f0 = [&](const uint32_t(&key)[U], const int(&)[U], unsigned vm) {
+    uint32_t d[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) d[j] = key[j] >> E::kShift0;
+    hist_add_vec<U>(h, d, vm);
+  };
   if (s.resident) {
     const int vb0 = s.lo < s.bl ? 1 : 0;
-    const int nbv = (s.bh - s.bl) / E::V;
+    const int nbv = (s.bh - s.bl) / (int)V;
     if (threadIdx.x == 0) {
       fence_proxy_async_smem();
+      const unsigned long long pol = policy_evict_first();
       for (int c = 0; c < kChunks; ++c) {
-        const int c0 = (int)((int64_t)nbv * c / kChunks), c1 = (int)((int64_t)nbv * (c + 1) / kChunks);
+        const int c0 = nbv * c / kChunks, c1 = nbv * (c + 1) / kChunks;
         if (c1 > c0) {
           const unsigned bytes = (unsigned)(c1 - c0) * 16u;
           mbar_arrive_expect_tx(&ctl->mbar[c], bytes);
           bulk_copy_g2s(sl + (size_t)(vb0 + c0) * 16, row + (int64_t)s.bl * E::ES + (int64_t)c0 * 16,
-                        bytes, &ctl->mbar[c]);
+                        bytes, &ctl->mbar[c], pol);
         }
       }
     }
@@ -450,11 +572,10 @@ __device__ bool select_row(const Params& p, int r, int part, unsigned char* smem
       E::store(sl + (size_t)(i - s.o) * E::ES, E::load(row, i));
     }
     __syncthreads();
-    auto f0 = [&](uint32_t key, int, bool valid) { hist_add(h, key >> E::kShift0, valid); };
     src.visit_vecs(0, vb0, f0);
     src.visit_vecs(vb0 + nbv, s.nvec, f0);
     for (int c = 0; c < kChunks; ++c) {
-      const int c0 = (int)((int64_t)nbv * c / kChunks), c1 = (int)((int64_t)nbv * (c + 1) / kChunks);
+      const int c0 = nbv * c / kChunks, c1 = nbv * (c + 1) / kChunks;
       if (c1 > c0) {
         mbar_wait_bounded(&ctl->mbar[c], (phase_bits >> c) & 1u, p.spin_limit_ns, ctl, status);
         phase_bits ^= 1u << c;
@@ -463,85 +584,135 @@ __device__ bool select_row(const Params& p, int r, int part, unsigned char* smem
     }
   } else {
     __syncthreads();
-    src.visit_global([&](uint32_t key, int, bool valid) { hist_add(h, key >> E::kShift0, valid); });
+    src.visit_global(f0);
   }
   __syncthreads();
   if (!ctl->ok) return false;
 
-  // ---- digit rounds until the threshold bin is small or exact ----
-  Prefix P = {0u, 0u, 0u, 0u};
-  unsigned k_rem = k;
+  // Counters of this call's parity; the other parity's are cleared below.
+  const unsigned epoch = hdr.x, par = epoch & 1u;
+  const unsigned used_other = par ? hdr.y : hdr.z;
+  unsigned* slot_hist = nullptr;
+  uint2* slot_cand = nullptr;
+  if (group > 1) {
+    slot_hist = reinterpret_cast<unsigned*>(reinterpret_cast<unsigned char*>(slot) + kSlotHistOff) +
+                (size_t)par * kSlotHistWords;
+    slot_cand = reinterpret_cast<uint2*>(p.ws + kWsHeaderBytes + (size_t)p.slots * kSlotBytes +
+                                         (size_t)(blockIdx.x / group) * kCandSlotBytes);
+  }
+
+  // ---- digit rounds: merge, threshold, emit; until the threshold bin is
+  //      taken whole or is small enough to finish on one block ----
+  Prefix P = {0u, 0u, 0u, 0u};  // resolved digits before round t
+  unsigned k_rem = k;           // still to select among elements matching P
+  unsigned base = 0;            // output slots already assigned to earlier rounds
   int t = 0;
-  bool collect = false;
+  int end = kEndAbove;
+  unsigned cnt = 0;
   const unsigned cap = group > 1 ? (unsigned)kGroupCandCap : (unsigned)kLocalCandCap;
+  uint2* cand = group > 1 ? slot_cand : lcand;
   for (;;) {
     const Digit D = digit_of_round<DT>(t, pos_bits);
     const int nb = 1 << D.bits;
     if (t > 0) {
-      zero_hist(h, nb);
+      zero_counters(h, nb);
       __syncthreads();
       hist_round(src, h, P, D, pmax);
       __syncthreads();
     }
     if (group > 1) {
       const bool skip = p.test_skip_arrive && part == 0 && t == 0;
-      if (!group_merge(h, nb, slot_hist + (size_t)t * kMaxBins, slot, (unsigned)group * (t + 1), skip,
-                       p.spin_limit_ns, ctl, status))
+      if (!group_merge(h, offs, nb, slot_hist + (size_t)t * kMaxBins, &slot->arrive[par],
+                       (unsigned)group * (t + 1), skip, p.spin_limit_ns, ctl, status))
         return false;
+      // every block of the call has read the epoch: the next call may use the other set
+      if (t == 0 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
+    } else {
+      zero_counters(offs, nb);
     }
-    unsigned bin, above, cnt;
+    unsigned bin, above;
     if (!pick_bin(h, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
+    const unsigned need = k_rem - above;
+    end = cnt == need ? kEndFinal : cnt <= cap ? kEndCollect : kEndAbove;
+    emit_round(src, P, D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
     prefix_extend(P, D, bin);
-    k_rem -= above;
-    if (cnt == k_rem) break;  // the whole bin is selected
-    if (cnt <= cap) {         // few enough to finish on one block
-      collect = true;
-      break;
-    }
+    base += above;
+    k_rem = need;
+    if (end != kEndAbove) break;
+    __syncthreads();
     if (++t >= nr) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return false;
     }
   }
 
-  // ---- collection ----
   if (group == 1) {
-    emit(src, P, pmax, collect, Reserve{nullptr}, out_row, k, lcand, cap, ctl, status);
-    if (collect) {
-      const unsigned n = min(ctl->cand_count, cap);
-      finish_on_chip<DT>(lcand, n, k_rem, P, t + 1, pos_bits, pmax, h, out_row, k, ctl, status);
+    if (end == kEndCollect) {
+      __syncthreads();
+      uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
+      for (unsigned i = threadIdx.x; i < cnt; i += kThreads) {
+        const uint2 e = lcand[i];
+        const uint32_t inv = pmax - e.y;
+        ok_ |= e.x; ak &= e.x; oi |= inv; ai &= inv;
+      }
+      block_or_and(ok_, ak, oi, ai, ctl);
+      finish_on_chip(lcand, cnt, k_rem, P, ok_, ak, oi, ai, pmax, h, out_row, k, ctl, status);
     }
     return true;
   }
 
-  emit(src, P, pmax, collect, Reserve{&slot->alloc}, out_row, k, slot_cand, cap, ctl, status);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(&slot->done, 1u);
-    ctl->is_last = (old == (unsigned)group - 1u) ? 1u : 0u;
-    if (ctl->is_last) __threadfence();
-  }
-  __syncthreads();
-  if (!ctl->is_last) return true;
-
-  // The last block of the row: finish the candidates, then reset the slot.
-  if (collect) {
-    const unsigned long long a = ld_cg_u64(&slot->alloc);
-    const unsigned n = min((unsigned)(a >> 32), cap);
-    uint2* fc = reinterpret_cast<uint2*>(sl);  // this block's slice copy is no longer needed
-    for (unsigned i = threadIdx.x; i < n; i += kThreads) fc[i] = ld_cg_u2(slot_cand + i);
-    if (threadIdx.x == 0) {
-      ctl->out_count = (unsigned)a;
-      ctl->cand_count = 0u;
+  // ---- rows split over blocks ----
+  if (part == 0) {
+    if (end == kEndCollect) {
+      // Gather the row's candidates as they land (each slot starts as all
+      // ones), put the slots back to all ones for the next call, then finish.
+      uint2* fc = reinterpret_cast<uint2*>(sl);  // this block's slice copy is no longer needed
+      unsigned long long* gc = reinterpret_cast<unsigned long long*>(slot_cand);
+      uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
+      const unsigned long long t0 = globaltimer_ns();
+      for (unsigned i0 = 0; i0 < cnt; i0 += 8u * kThreads) {
+        unsigned long long e[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const unsigned i = i0 + j * kThreads + threadIdx.x;
+          e[j] = i < cnt ? ld_relaxed_u64(gc + i) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const unsigned i = i0 + j * kThreads + threadIdx.x;
+          if (i >= cnt) continue;
+          while (e[j] == kCandEmpty) {
+            if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+              ctl->ok = 0u;
+              atomicOr(status, kStatTimeout);
+              break;
+            }
+            e[j] = ld_relaxed_u64(gc + i);
+          }
+          const uint2 c2 = make_uint2((uint32_t)e[j], (uint32_t)(e[j] >> 32));
+          fc[i] = c2;
+          gc[i] = kCandEmpty;
+          const uint32_t inv = pmax - c2.y;
+          ok_ |= c2.x; ak &= c2.x; oi |= inv; ai &= inv;
+        }
+      }
+      block_or_and(ok_, ak, oi, ai, ctl);
+      if (!ctl->ok) return false;
+      finish_on_chip(fc, cnt, k_rem, P, ok_, ak, oi, ai, pmax, h, out_row, k, ctl, status);
     }
-    __syncthreads();
-    finish_on_chip<DT>(fc, n, k_rem, P, t + 1, pos_bits, pmax, h, out_row, k, ctl, status);
-  }
-  for (int i = threadIdx.x; i < (t + 1) * kMaxBins; i += kThreads) slot_hist[i] = 0u;
-  if (threadIdx.x == 0) {
-    slot->arrive = 0u;
-    slot->done = 0u;
-    slot->alloc = 0ull;
+    if (threadIdx.x == 0) slot->used[par] = (unsigned)(t + 1);
+  } else {
+    // Clear the other parity's counters, used by the previous call on this
+    // slot, for the next one; the blocks other than the finisher share it.
+    const unsigned helpers = (unsigned)group - 1u, me = (unsigned)part - 1u;
+    unsigned* other = reinterpret_cast<unsigned*>(reinterpret_cast<unsigned char*>(slot) + kSlotHistOff) +
+                      (size_t)(par ^ 1u) * kSlotHistWords;
+    const unsigned words = min(used_other, (unsigned)kMaxRounds) * (unsigned)kMaxBins;
+    const unsigned per = ((words / 4 + helpers - 1) / helpers) * 4;
+    const unsigned w0 = min(words, me * per), w1 = min(words, w0 + per);
+    for (unsigned i = w0 / 4 + threadIdx.x; i < w1 / 4; i += kThreads)
+      reinterpret_cast<uint4*>(other)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (me == 0 && threadIdx.x == 0) slot->arrive[par ^ 1u] = 0u;
   }
   return true;
 }
@@ -579,6 +750,7 @@ struct DeviceInfo {
 struct Workspace {
   unsigned char* ptr = nullptr;
   size_t bytes = 0;
+  int slots = 0;
 };
 
 std::mutex g_mu;
@@ -648,8 +820,19 @@ void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* gr
   *grid = batch * (int)g;
 }
 
+int workspace_slots(const DeviceInfo& d) { return d.sms * d.blocks_per_sm; }
+
+// Layout: status header | slot headers and counters | candidate slots.
 size_t workspace_bytes(const DeviceInfo& d) {
-  return kWsHeaderBytes + (size_t)d.sms * d.blocks_per_sm * kSlotBytes;
+  return kWsHeaderBytes + (size_t)workspace_slots(d) * (kSlotBytes + kCandSlotBytes);
+}
+
+// Counters start at zero, candidate slots at all ones ("not written").
+cudaError_t workspace_clear(const Workspace& w, int slots, cudaStream_t stream) {
+  const size_t zero_bytes = kWsHeaderBytes + (size_t)slots * kSlotBytes;
+  cudaError_t e = cudaMemsetAsync(w.ptr, 0, zero_bytes, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w.ptr + zero_bytes, 0xFF, w.bytes - zero_bytes, stream);
+  return e;
 }
 
 int get_workspace(int dev, void* stream, const DeviceInfo& d, Workspace* out) {
@@ -661,11 +844,12 @@ int get_workspace(int dev, void* stream, const DeviceInfo& d, Workspace* out) {
   }
   Workspace w;
   w.bytes = workspace_bytes(d);
+  w.slots = workspace_slots(d);
   if (cudaMalloc(&w.ptr, w.bytes) != cudaSuccess) {
     cudaGetLastError();
     return TKS_E_CUDA;
   }
-  if (cudaMemsetAsync(w.ptr, 0, w.bytes, (cudaStream_t)stream) != cudaSuccess) {
+  if (workspace_clear(w, w.slots, (cudaStream_t)stream) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(w.ptr);
     return TKS_E_CUDA;
@@ -720,6 +904,7 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
   p.group = group;
   p.test_skip_arrive = g_test_skip_arrive.load() ? 1 : 0;
   p.ws = w.ptr;
+  p.slots = w.slots;
   p.spin_limit_ns = g_spin_limit_ns.load();
 
   cudaLaunchConfig_t cfg;
@@ -771,7 +956,7 @@ extern "C" int tks_device_status(void* stream) {
     return TKS_E_CUDA;
   }
   if (st == 0) return TKS_OK;
-  if (cudaMemsetAsync(w.ptr, 0, w.bytes, (cudaStream_t)stream) != cudaSuccess ||
+  if (workspace_clear(w, w.slots, (cudaStream_t)stream) != cudaSuccess ||
       cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
     cudaGetLastError();
     return TKS_E_CUDA;
