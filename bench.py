@@ -1,0 +1,441 @@
+"""Benchmark of the top-k index selector.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode_1m_masked]
+
+A step is one tks_topk_indices call over one batch of the named workload
+(batch=1, N=1048576 fp32 logits, k=2048 by default).  Steps read rotating
+copies of the input whose total size exceeds twice the L2 cache, so every
+step reads its logits from HBM.  K steps are captured in CUDA graphs and
+timed with CUDA events on the launching stream.
+
+Prints one JSON line.  `value` is microseconds per row over the whole job
+(lower is better).  `roofline` compares the one-pass algorithmic read bytes
+per launch with the measured HBM copy bandwidth.  `e2e` repeats the
+measurement through the public API with host buffers (pinned host -> device
+copy of the logits, the call, device -> host copy of the indices) inside the
+timed region.  `cpu_baseline` times the CPU oracle on a bounded sample.
+
+--impl reference times the CPU oracle itself (the only reference that exists
+for this method) on the same workload, as a bounded sample per step.
+
+With torchrun (--gpus N > 1) every rank runs an independent replica on its
+own GPU (rows are independent; there is no data exchange); the time is the
+maximum over ranks and `value` divides it by the rows all ranks processed.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "TopK-select µs/row and HBM GB/s (batch=1, N=128K–1M, k=2048) vs roofline"
+UNIT = "us/row"
+KERNEL_SOURCES = [
+    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_select.cu"),
+    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_device.cuh"),
+]
+PROFILES = os.path.join(ROOT, "profiles")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(PROFILES, f"tks_select_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
+    m_tr = re.search(r"dram bytes per launch:\s*([0-9]+)", text)
+    if not (m_hash and m_tr) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if (device is not None and dist.get_backend() == "nccl") else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as baseline
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_time(w, budget_s: float = 10.0) -> dict:
+    """The oracle (single thread) on whole rows of the workload, repeated
+    until about budget_s of CPU work; microseconds per row."""
+    import oracle
+    lib = oracle.load()
+    times = []
+    t_start = time.perf_counter()
+    r = 0
+    while True:
+        row = r % w.batch
+        L = int(w.row_len[row])
+        t0 = time.perf_counter()
+        oracle.topk_indices(w.values[row:row + 1, :L], w.k, None, w.dtype, lib=lib)
+        times.append(time.perf_counter() - t0)
+        r += 1
+        if time.perf_counter() - t_start > budget_s and r >= 3:
+            break
+    return {"value": round(statistics.median(times) * 1e6, 3), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{r} whole rows of {w.name} (N={int(w.row_len[0])}), median of single-thread "
+                      f"C oracle runs on {os.cpu_count()} host cores (1 used)"}
+
+
+def reference_arm(args, w):
+    """--impl reference: the CPU oracle per step on a bounded prefix sample of
+    the row, scaled to a whole row by n log n."""
+    import oracle
+    lib = oracle.load()
+    steps, warmup = args.steps, args.warmup
+    budget = 90.0  # seconds for the whole run
+    N = int(w.row_len[0])
+    # one full-row timing fixes the per-element cost, then size the sample
+    t0 = time.perf_counter()
+    oracle.topk_indices(w.values[0:1, :N], w.k, None, w.dtype, lib=lib)
+    full = time.perf_counter() - t0
+    per = budget / max(1, steps + warmup)
+    n = N
+    while n > 4096 and full * (n * math.log2(n)) / (N * math.log2(N)) > per:
+        n //= 2
+    kk = min(w.k, max(1, n // 8))
+    sample = w.values[0:1, :n]
+    for _ in range(warmup):
+        oracle.topk_indices(sample, kk, None, w.dtype, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.topk_indices(sample, kk, None, w.dtype, lib=lib)
+    dt = time.perf_counter() - t0
+    scale = (N * math.log2(N)) / (n * math.log2(n))
+    us_row = dt / steps * 1e6 * scale
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us_row, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": warmup, "ms_per_step": round(us_row / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "n": N, "k": w.k},
+        "cpu_baseline": {"value": round(us_row, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {n} positions of the row, k={kk}, per step; "
+                                   f"scaled to N={N} by n*log2(n) (merge sort)"},
+        "e2e": {"value": round(us_row, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_arm(args, w, dist, rank, world, device):
+    import torch
+
+    import sparse_attention_topk_gb300 as tks
+
+    tks.load()
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    x_host = torch.from_numpy(w.values.copy())
+    if w.dtype == W.BF16:
+        x_host = x_host.view(torch.bfloat16)
+    nbytes = x_host.numel() * x_host.element_size()
+    ncopies = max(2, math.ceil(2.5 * l2 / nbytes))
+    base = x_host.to(device)
+    copies = [base.clone() for _ in range(ncopies)]
+    full_rows = bool(np.all(w.row_len == w.row_stride))
+    rl = None if full_rows else torch.from_numpy(w.row_len.copy()).to(device)
+    out = torch.empty((w.batch, w.k), dtype=torch.int32, device=device)
+
+    def call(i):
+        tks.topk_indices(copies[i % ncopies], w.k, row_len=rl, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call(0)  # sets up the stream's workspace before capture
+    stream.synchronize()
+    st = tks.device_status(stream)
+    if st != tks.TKS_OK:
+        raise RuntimeError(f"device status after set-up: {tks.status_string(st)}")
+
+    G = min(512, args.steps)
+
+    def capture(n, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                call(offset + i)
+        return g
+
+    g_full = capture(G, 0)
+    tail = args.steps % G
+    g_tail = capture(tail, 0) if tail else None
+
+    def run_steps(k):
+        with torch.cuda.stream(stream):
+            for _ in range(k // G):
+                g_full.replay()
+            if k % G:
+                (g_tail if k % G == tail and g_tail is not None else capture(k % G, 0)).replay()
+
+    # warm-up: W steps
+    run_steps(max(3, args.warmup))
+    stream.synchronize()
+
+    # timed: exactly K steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid or device.index)
+    with ClockSampler(gpu_id) as clk:
+        e0.record(stream)
+        run_steps(args.steps)
+        e1.record(stream)
+        e1.synchronize()
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    ms = e0.elapsed_time(e1)
+    st = tks.device_status(stream)
+    if st != tks.TKS_OK:
+        raise RuntimeError(f"device status after the timed run: {tks.status_string(st)}")
+    ms_max = max_over_ranks(dist, ms, device)
+
+    rows_total = args.steps * w.batch * world
+    us_per_row = ms_max * 1e3 / rows_total
+    launch_us = ms * 1e3 / args.steps  # one kernel launch per step on this rank
+    alg_bytes = w.algorithmic_bytes
+    achieved = alg_bytes / (launch_us * 1e-6) / 1e9
+    peak, peak_src = measured_peaks()
+
+    # end to end through the public API with host buffers
+    k_e2e = min(args.steps, 2000)
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
+    x_dev = torch.empty_like(base)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_pin, non_blocking=True)
+            tks.topk_indices(x_dev, w.k, row_len=rl, out=out, stream=stream)
+            out_pin.copy_(out, non_blocking=True)
+    stream.synchronize()
+    barrier(dist, device)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(k_e2e):
+            x_dev.copy_(x_pin, non_blocking=True)
+            tks.topk_indices(x_dev, w.k, row_len=rl, out=out, stream=stream)
+            out_pin.copy_(out, non_blocking=True)
+    f1.record(stream)
+    f1.synchronize()
+    barrier(dist, device)
+    e2e_ms = max_over_ranks(dist, f0.elapsed_time(f1), device)
+    e2e_us_row = e2e_ms * 1e3 / (k_e2e * w.batch * world)
+
+    # the result of the last step is correct (cheap spot check on rank 0)
+    if rank == 0:
+        import oracle
+        want = oracle.topk_workload(w)
+        got = np.sort(out_pin.numpy(), axis=1)
+        if not np.array_equal(got, want):
+            raise RuntimeError("GPU result differs from the oracle")
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(us_per_row, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.batch, "n": int(w.row_stride), "k": w.k,
+            "logits": w.dtype, "row_len": "full rows" if full_rows else "ragged (device row_len)",
+            "l2": f"inputs larger than L2: {ncopies} rotating copies of {nbytes} B "
+                  f"({ncopies * nbytes / 2**20:.0f} MiB > 2x {l2 / 2**20:.0f} MiB L2)",
+            "graph": f"{G} calls per CUDA graph", "parallelism": f"replicas x{world}",
+            "plan": dict(zip(("blocks_per_row", "grid"), tks.plan(w.batch, w.row_stride, w.k,
+                                                                  0 if w.dtype == W.F32 else 1))),
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 5), "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "traffic": recorded_traffic(w.name),
+        },
+        "gpu_launches": args.steps,
+        "e2e": {"value": round(e2e_us_row, 4), "unit": UNIT,
+                "h2d_bytes_per_step": int(nbytes), "d2h_bytes_per_step": int(w.batch * w.k * 4),
+                "steps": k_e2e},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world >= 1:
+        line["cpu_baseline"] = cpu_oracle_time(w, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_1m_masked", choices=sorted(W.NAMED))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of CPU oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_env()
+    w = W.named(args.workload)
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, w)
+        return 0
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the CPU oracle alone: --impl reference)")
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    try:
+        gpu_arm(args, w, dist, rank, world, device)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

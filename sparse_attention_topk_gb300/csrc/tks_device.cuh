@@ -292,23 +292,20 @@ __device__ __forceinline__ void ranks_vec(unsigned* counter, unsigned sel, unsig
   for (int j = 0; j < U; ++j) o[j] = base + mine[j];
 }
 
-// Histogram update for U elements per lane (one vote per call): if every
-// lane's U elements are valid and share lane 0's bin, lane 0 adds 32*U once
-// (constant and plateau rows); otherwise every valid element adds 1 with
-// independent atomics.
+// Histogram update for U elements per lane.  A lane whose U elements are all
+// valid and share one bin adds U once (constant and plateau rows); otherwise
+// every valid element adds 1.  Each add is a predicated atomic, so there is
+// no branch and no vote.
 template <int U>
 __device__ __forceinline__ void hist_add_vec(unsigned* h, const uint32_t (&d)[U], unsigned vm) {
   constexpr unsigned kAll = (1u << U) - 1u;
-  bool uni = vm == kAll;
+  bool run = vm == kAll;
 #pragma unroll
-  for (int j = 1; j < U; ++j) uni &= d[j] == d[0];
-  const uint32_t d0 = __shfl_sync(0xffffffffu, d[0], 0);
-  if (__all_sync(0xffffffffu, uni && d[0] == d0)) {
-    if (lane_id() == 0) atomicAdd(&h[d0], 32u * U);
-  } else {
+  for (int j = 1; j < U; ++j) run &= d[j] == d[0];
 #pragma unroll
-    for (int j = 0; j < U; ++j)
-      if ((vm >> j) & 1u) atomicAdd(&h[d[j]], 1u);
+  for (int j = 0; j < U; ++j) {
+    const unsigned add = run ? (j == 0 ? (unsigned)U : 0u) : ((vm >> j) & 1u);
+    if (add) atomicAdd(&h[d[j]], add);
   }
 }
 

@@ -130,21 +130,27 @@ struct SliceSrc {
     f(key, pos, vm);
   }
 
-  // 16-byte vectors [va, vb) of the on-chip copy.
+  // 16-byte vectors [va, vb) of the on-chip copy, two in flight per lane.
   template <class F>
   __device__ __forceinline__ void visit_vecs(int va, int vb, F&& f) const {
-    for (int v0 = va; v0 < vb; v0 += kThreads) {
-      const int v = v0 + (int)threadIdx.x;
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      unsigned vm = 0u;
-      if (v < vb) {
-        x = reinterpret_cast<const uint4*>(sm)[v];
-        const int i0 = s.o + v * U;
-        vm = (1u << U) - 1u;
-        if (i0 < s.lo) vm &= ~0u << (s.lo - i0);
-        if (i0 + U > s.hi) vm &= (1u << max(0, s.hi - i0)) - 1u;
+    for (int v0 = va; v0 < vb; v0 += 2 * kThreads) {
+      uint4 x[2];
+      unsigned vm[2];
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int v = v0 + a * kThreads + (int)threadIdx.x;
+        x[a] = make_uint4(0u, 0u, 0u, 0u);
+        vm[a] = 0u;
+        if (v < vb) {
+          x[a] = reinterpret_cast<const uint4*>(sm)[v];
+          const int i0 = s.o + v * U;
+          vm[a] = (1u << U) - 1u;
+          if (i0 < s.lo) vm[a] &= ~0u << (s.lo - i0);
+          if (i0 + U > s.hi) vm[a] &= (1u << max(0, s.hi - i0)) - 1u;
+        }
       }
-      vec(x, s.o + v * U, vm, f);
+      vec(x[0], s.o + (v0 + (int)threadIdx.x) * U, vm[0], f);
+      if (v0 + kThreads < vb) vec(x[1], s.o + (v0 + kThreads + (int)threadIdx.x) * U, vm[1], f);
     }
   }
 
@@ -230,12 +236,33 @@ __device__ __forceinline__ void zero_counters(unsigned* h, int n) {
   for (int i = threadIdx.x; i < (n + 3) / 4; i += kThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Largest and smallest valid key of a lane's U elements (0 / ~0 if none).
+template <int U>
+__device__ __forceinline__ void key_range(const uint32_t (&key)[U], unsigned vm, uint32_t* mx,
+                                          uint32_t* mn) {
+  uint32_t a = 0u, b = ~0u;
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    const bool v = (vm >> j) & 1u;
+    a = max(a, v ? key[j] : 0u);
+    b = min(b, v ? key[j] : ~0u);
+  }
+  *mx = a;
+  *mn = b;
+}
+
 // Histogram of digit D over the elements that match the prefix.
 template <class Src>
 __device__ __forceinline__ void hist_round(const Src& src, unsigned* h, const Prefix& P, Digit D,
                                            uint32_t pmax) {
   constexpr int U = Src::U;
   src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+    // the value-key prefix is monotone in the key: skip vectors with no
+    // element inside it (one vote)
+    uint32_t mx, mn;
+    key_range<U>(key, vm, &mx, &mn);
+    const bool none = vm == 0u || (mx & P.kmask) < P.kpref || (mn & P.kmask) > P.kpref;
+    if (__all_sync(0xffffffffu, none)) return;
     uint32_t d[U];
     unsigned m = 0u;
 #pragma unroll
@@ -244,7 +271,7 @@ __device__ __forceinline__ void hist_round(const Src& src, unsigned* h, const Pr
       if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0) m |= 1u << j;
       d[j] = digit_value(D, key[j], inv);
     }
-    if (__any_sync(0xffffffffu, m != 0u)) hist_add_vec<U>(h, d, m);
+    hist_add_vec<U>(h, d, m);
   });
 }
 
@@ -268,7 +295,7 @@ __device__ __forceinline__ void mbar_wait_bounded(unsigned long long* bar, unsig
 // offs[] to place the block's elements in the output later without any
 // further coordination.  Then a bounded barrier over the row's blocks, then
 // the row's summed counts replace the local ones in h[].
-__device__ bool group_merge(unsigned* h, unsigned* offs, int nb, unsigned* g, unsigned* arrive,
+__device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int nb, unsigned* g, unsigned* arrive,
                             unsigned target, bool skip_arrive, long long limit, Ctl* ctl,
                             unsigned* status) {
   constexpr int kPer = kMaxBins / kThreads;
@@ -362,13 +389,24 @@ __device__ __forceinline__ void put_cand(uint2* cand, unsigned i, uint32_t key, 
 // the rank coming from this block's running offset offs[bin]; candidates go
 // to cand[offs[bin]++].
 template <class Src>
-__device__ void emit_round(const Src& src, const Prefix& P, Digit D, unsigned bin, int end,
+__device__ __forceinline__ void emit_round(const Src& src, const Prefix& P, Digit D, unsigned bin, int end,
                            unsigned base, const unsigned* suf, unsigned* offs, uint32_t pmax,
                            int32_t* out_row, unsigned k, uint2* cand, bool cand_global,
                            unsigned cap, unsigned* status) {
   constexpr int U = Src::U;
   bool bad = false;
+  // Every emitted element has (key & qmask) >= qval, and that part of the
+  // key is monotone in the key: vectors whose largest key fails it are
+  // skipped with one vote.
+  uint32_t qmask = P.kmask, qval = P.kpref;
+  if (!D.on_pos) {
+    qmask |= ((1u << D.bits) - 1u) << D.shift;
+    qval |= bin << D.shift;
+  }
   src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+    uint32_t mx, mn;
+    key_range<U>(key, vm, &mx, &mn);
+    if (__all_sync(0xffffffffu, vm == 0u || (mx & qmask) < qval)) return;
     uint32_t d[U];
     unsigned sel = 0u, to_cand = 0u;
 #pragma unroll
@@ -421,7 +459,7 @@ __device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, Digit* D)
 // equal in every candidate join the prefix at once; digits are taken from the
 // highest bits that still differ, so no round is spent on a constant digit.
 // (or_*, and_*: OR and AND of the candidates' keys and inverted positions.)
-__device__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Prefix P,
+__device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Prefix P,
                                uint32_t or_k, uint32_t and_k, uint32_t or_i, uint32_t and_i,
                                uint32_t pmax, unsigned* h, int32_t* out_row, unsigned k, Ctl* ctl,
                                unsigned* status) {
@@ -479,7 +517,7 @@ __device__ void finish_on_chip(const uint2* cand, unsigned n, unsigned k_rem, Pr
 // Selects the top k of row r with this block as part `part` of `group`.
 // Returns false after an unrecoverable device-side error.
 template <int DT>
-__device__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
+__device__ __forceinline__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
                            unsigned& phase_bits) {
   using E = Elt<DT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
