@@ -47,7 +47,8 @@ typedef enum {
     TKS_E_CUDA = 3,        /* a CUDA runtime call failed (allocation, launch) */
     TKS_E_TIMEOUT = 4,     /* a device-side wait between thread blocks gave up */
     TKS_E_INTERNAL = 5,    /* a device-side consistency check failed */
-    TKS_E_ROW_LEN = 6      /* a device row length was < 0 or > row_stride (clamped) */
+    TKS_E_ROW_LEN = 6,     /* a device row length was < 0 or > row_stride (clamped) */
+    TKS_E_TOO_LARGE = 7    /* more rows than tks_topk_indices_noalloc's fixed scratch holds */
 } tks_status;
 
 /* Largest k accepted. */
@@ -137,6 +138,35 @@ int tks_set_option(int option, int64_t value);
  */
 int tks_plan(int32_t batch, int64_t row_stride, int32_t k, int32_t dtype, int32_t *group,
              int32_t *grid);
+
+/*
+ * tks_topk_indices_noalloc - the same selection as tks_topk_indices, for
+ * callers that cannot allocate device memory: code that runs where a
+ * cudaMalloc is not allowed or not wanted (inside a pre-planned memory pool,
+ * under an allocator that must not grow, or from a runtime that forbids
+ * allocation after start-up).  The papers this library follows have no
+ * counterpart to it; it exists only for such callers.
+ *
+ * Arguments, result layout and argument errors are those of
+ * tks_topk_indices; the caller still provides logits, row_len and out_idx.
+ * Instead of a workspace, the call uses a fixed scratch array compiled into
+ * the library (about 2.9 MB, present on every device that loads the library
+ * until the process exits).  That array holds at most TKS_NOALLOC_MAX_ROWS
+ * rows: a larger batch returns TKS_E_TOO_LARGE and launches nothing.  The call
+ * makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any CUDA-graph capture.  Every
+ * call clears the part of the array it uses before its kernel runs, on
+ * `stream`.  All calls share the one array, so calls that overlap on the GPU
+ * (on different streams, or from several threads) race and give wrong
+ * results: serialise them.  Device-side errors of this entry point are not
+ * reported by tks_device_status (which covers the allocating entry point).
+ */
+#define TKS_NOALLOC_MAX_ROWS 8
+int tks_topk_indices_noalloc(const void *logits, const int32_t *row_len, int32_t batch,
+                             int64_t row_stride, int32_t k, int32_t dtype, int32_t *out_idx,
+                             void *stream);
 
 #ifdef __cplusplus
 }

@@ -28,6 +28,8 @@ TKS_E_CUDA = 3
 TKS_E_TIMEOUT = 4
 TKS_E_INTERNAL = 5
 TKS_E_ROW_LEN = 6
+TKS_E_TOO_LARGE = 7
+TKS_NOALLOC_MAX_ROWS = 8
 
 TKS_K_MAX = 1 << 24
 
@@ -46,6 +48,7 @@ SIGNATURES = {
     "tks_release": (ctypes.c_int, []),
     "tks_set_option": (ctypes.c_int, [ctypes.c_int, _I64]),
     "tks_plan": (ctypes.c_int, [_I32, _I64, _I32, _I32, _VP, _VP]),
+    "tks_topk_indices_noalloc": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
 }
 
 _lock = threading.Lock()
@@ -129,6 +132,17 @@ def topk_indices_raw(logits_ptr: int, row_len_ptr: int | None, batch: int, row_s
         ctypes.c_void_p(stream_handle or 0)))
 
 
+def topk_indices_noalloc_raw(logits_ptr: int, row_len_ptr: int | None, batch: int,
+                             row_stride: int, k: int, dtype: int, out_ptr: int,
+                             stream_handle: int | None = None) -> int:
+    """Direct call of tks_topk_indices_noalloc (no device allocation; at most
+    TKS_NOALLOC_MAX_ROWS rows; calls must not overlap on the GPU)."""
+    return int(load().tks_topk_indices_noalloc(
+        ctypes.c_void_p(logits_ptr), ctypes.c_void_p(row_len_ptr or 0), int(batch),
+        int(row_stride), int(k), int(dtype), ctypes.c_void_p(out_ptr),
+        ctypes.c_void_p(stream_handle or 0)))
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
         import torch
@@ -188,9 +202,10 @@ def topk_indices(logits, k: int, row_len=None, out=None, stream=None):
 
 
 __all__ = [
-    "topk_indices", "topk_indices_raw", "device_status", "set_option", "plan", "release",
+    "topk_indices", "topk_indices_raw", "topk_indices_noalloc_raw", "device_status", "set_option", "plan", "release",
     "status_string", "version", "load", "lib_path", "build", "TksError", "SIGNATURES",
     "TKS_F32", "TKS_BF16", "TKS_OK", "TKS_E_INVAL", "TKS_E_UNSUPPORTED", "TKS_E_CUDA",
-    "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_K_MAX", "TKS_OPT_FORCE_GROUP",
+    "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_E_TOO_LARGE", "TKS_NOALLOC_MAX_ROWS",
+    "TKS_K_MAX", "TKS_OPT_FORCE_GROUP",
     "TKS_OPT_SPIN_LIMIT_NS", "TKS_OPT_MIN_PER_BLOCK", "TKS_OPT_TEST_SKIP_ARRIVE",
 ]

@@ -1013,6 +1013,7 @@ extern "C" const char* tks_status_string(int status) {
     case TKS_E_TIMEOUT: return "a device-side wait between thread blocks timed out";
     case TKS_E_INTERNAL: return "device-side consistency check failed";
     case TKS_E_ROW_LEN: return "a row length was outside [0, row_stride] and was clamped";
+    case TKS_E_TOO_LARGE: return "more rows than the allocation-free entry point's fixed scratch holds";
     default: return "unknown status";
   }
 }
@@ -1064,5 +1065,108 @@ extern "C" int tks_plan(int32_t batch, int64_t row_stride, int32_t k, int32_t dt
   plan_launch(d, batch, row_stride, &g, &gr);
   if (group) *group = g;
   if (grid) *grid = gr;
+  return TKS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.  Same selection, but its scratch (status word,
+// per-row counters, candidate words) lives in a fixed array compiled into this
+// library instead of a workspace the library allocates.
+// ---------------------------------------------------------------------------
+namespace tks {
+namespace {
+constexpr size_t kNoAllocBytes =
+    kWsHeaderBytes + (size_t)TKS_NOALLOC_MAX_ROWS * (kSlotBytes + kCandSlotBytes);
+std::map<int, unsigned char*> g_noalloc_addr;  // device -> device address of the array
+}  // namespace
+}  // namespace tks
+
+// About 2.9 MB on every device that loads this library, held until exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[tks::kNoAllocBytes];
+
+extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_len, int32_t batch,
+                                        int64_t row_stride, int32_t k, int32_t dtype,
+                                        int32_t* out_idx, void* stream) {
+  if (batch < 0 || row_stride < 0 || row_stride > INT32_MAX || k < 1 || k > TKS_K_MAX)
+    return TKS_E_INVAL;
+  if (dtype != TKS_F32 && dtype != TKS_BF16) return TKS_E_INVAL;
+  if (batch == 0) return TKS_OK;
+  if (batch > TKS_NOALLOC_MAX_ROWS) return TKS_E_TOO_LARGE;
+  const int es = dtype == TKS_F32 ? 4 : 2;
+  if (out_idx == nullptr || ((uintptr_t)out_idx & 3u) != 0) return TKS_E_INVAL;
+  if (row_stride > 0 && (logits == nullptr || ((uintptr_t)logits % (uintptr_t)es) != 0))
+    return TKS_E_INVAL;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TKS_E_UNSUPPORTED;
+  }
+  DeviceInfo d;
+  unsigned char* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const int rc = device_info(dev, &d);
+    if (rc != TKS_OK) return rc;
+    auto it = g_noalloc_addr.find(dev);
+    if (it == g_noalloc_addr.end()) {
+      // Host code only sees a stand-in for the array; its device address is
+      // looked up once per device, with that device current.
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return TKS_E_CUDA;
+      }
+      it = g_noalloc_addr.emplace(dev, static_cast<unsigned char*>(ptr)).first;
+    }
+    ws = it->second;
+  }
+  int group = 1, grid = 1;
+  plan_launch(d, batch, row_stride, &group, &grid);
+
+  // The array keeps whatever the previous call left: clear the status word and
+  // the counters of the rows used, and mark their candidate words unwritten.
+  const cudaStream_t s = (cudaStream_t)stream;
+  const size_t zero_bytes = kWsHeaderBytes + (group > 1 ? (size_t)batch * kSlotBytes : 0);
+  if (cudaMemsetAsync(ws, 0, zero_bytes, s) != cudaSuccess ||
+      (group > 1 && cudaMemsetAsync(ws + kWsHeaderBytes + (size_t)TKS_NOALLOC_MAX_ROWS * kSlotBytes, 0xFF,
+                                    (size_t)batch * kCandSlotBytes, s) != cudaSuccess)) {
+    cudaGetLastError();
+    return TKS_E_CUDA;
+  }
+
+  Params p;
+  p.logits = static_cast<const unsigned char*>(logits);
+  p.row_len = row_len;
+  p.row_stride = row_stride;
+  p.batch = batch;
+  p.k = k;
+  p.out = out_idx;
+  p.group = group;
+  p.test_skip_arrive = 0;
+  p.ws = ws;
+  p.slots = TKS_NOALLOC_MAX_ROWS;
+  p.spin_limit_ns = g_spin_limit_ns.load();
+
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  std::memset(attr, 0, sizeof attr);
+  if (group > 1) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0>, p)
+                                         : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TKS_E_CUDA;
+  }
   return TKS_OK;
 }
