@@ -246,70 +246,6 @@ __device__ __forceinline__ unsigned block_suffix_excl(unsigned v, unsigned* tota
 }
 
 // ---------------------------------------------------------------------------
-// Counters updated by whole warps.
-// ---------------------------------------------------------------------------
-
-// Output slots for U elements per lane: o[j] = old value of c[d[j]] after
-// adding 1 for every selected element.  A full warp whose selected elements
-// all share lane 0's counter takes its slots with one add; otherwise the
-// selected elements add independently (no chain of votes per element).
-template <int U>
-__device__ __forceinline__ void slots_vec(unsigned* c, const uint32_t (&d)[U], unsigned sel,
-                                          unsigned (&o)[U]) {
-  constexpr unsigned kAll = (1u << U) - 1u;
-  bool uni = sel == kAll;
-#pragma unroll
-  for (int j = 1; j < U; ++j) uni &= d[j] == d[0];
-  const uint32_t d0 = __shfl_sync(0xffffffffu, d[0], 0);
-  if (__all_sync(0xffffffffu, uni && d[0] == d0)) {
-    unsigned base = 0;
-    if (lane_id() == 0) base = atomicAdd(&c[d0], 32u * U);
-    base = __shfl_sync(0xffffffffu, base, 0) + lane_id() * U;
-#pragma unroll
-    for (int j = 0; j < U; ++j) o[j] = base + j;
-  } else {
-#pragma unroll
-    for (int j = 0; j < U; ++j) o[j] = ((sel >> j) & 1u) ? atomicAdd(&c[d[j]], 1u) : 0u;
-  }
-}
-
-// Ranks for U selected-or-not elements per lane against one shared counter:
-// one add per warp call, ranks from ballots.
-template <int U>
-__device__ __forceinline__ void ranks_vec(unsigned* counter, unsigned sel, unsigned (&o)[U]) {
-  const unsigned lt = (1u << lane_id()) - 1u;
-  unsigned before = 0, mine[U];
-#pragma unroll
-  for (int j = 0; j < U; ++j) {
-    const unsigned m = __ballot_sync(0xffffffffu, (sel >> j) & 1u);
-    mine[j] = before + (unsigned)__popc(m & lt);
-    before += (unsigned)__popc(m);
-  }
-  unsigned base = 0;
-  if (lane_id() == 0 && before) base = atomicAdd(counter, before);
-  base = __shfl_sync(0xffffffffu, base, 0);
-#pragma unroll
-  for (int j = 0; j < U; ++j) o[j] = base + mine[j];
-}
-
-// Histogram update for U elements per lane.  A lane whose U elements are all
-// valid and share one bin adds U once (constant and plateau rows); otherwise
-// every valid element adds 1.  Each add is a predicated atomic, so there is
-// no branch and no vote.
-template <int U>
-__device__ __forceinline__ void hist_add_vec(unsigned* h, const uint32_t (&d)[U], unsigned vm) {
-  constexpr unsigned kAll = (1u << U) - 1u;
-  bool run = vm == kAll;
-#pragma unroll
-  for (int j = 1; j < U; ++j) run &= d[j] == d[0];
-#pragma unroll
-  for (int j = 0; j < U; ++j) {
-    const unsigned add = run ? (j == 0 ? (unsigned)U : 0u) : ((vm >> j) & 1u);
-    if (add) atomicAdd(&h[d[j]], add);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Threshold scan over h[0..nb): the bin holding the k_rem-th largest element
 // (1-based), the count strictly above it and its own count.  Rewrites h in
 // place into exclusive suffix sums (h[i] = number of elements in bins > i),

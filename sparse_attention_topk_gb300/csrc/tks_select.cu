@@ -101,14 +101,17 @@ struct Slice {
   int bl, bh;  // 16-byte aligned body [bl, bh)
   int o;       // position held by byte 0 of the on-chip copy
   int nvec;    // 16-byte vectors of the on-chip copy
+  int vb0;     // first whole vector of the body in the on-chip copy (0 or 1)
+  int nbv;     // whole vectors in the body
   bool resident;
 };
 
 // ---------------------------------------------------------------------------
-// Element sources.  visit(f) hands each lane U elements at a time:
-// f(key[U], pos[U], vm), bit j of vm set when element j is real.  All 32
-// lanes of a warp call f together (f may vote once per call), and a thread
-// meets its elements in the same order on every visit.
+// Element sources.  visit(f) calls f(key[U], pos[U], vm) for groups of U
+// elements, bit j of vm set when element j is real.  Each thread walks its
+// own groups independently (f must not use warp-wide operations): shared
+// memory atomics on GB300 absorb same-address conflicts inside a warp, so a
+// plain strided loop with plain atomics is the fastest form of every pass.
 // ---------------------------------------------------------------------------
 template <int DT>
 struct SliceSrc {
@@ -130,28 +133,25 @@ struct SliceSrc {
     f(key, pos, vm);
   }
 
-  // 16-byte vectors [va, vb) of the on-chip copy, two in flight per lane.
+  // Whole vectors [va, vb) of the on-chip copy.
   template <class F>
-  __device__ __forceinline__ void visit_vecs(int va, int vb, F&& f) const {
-    for (int v0 = va; v0 < vb; v0 += 2 * kThreads) {
-      uint4 x[2];
-      unsigned vm[2];
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int v = v0 + a * kThreads + (int)threadIdx.x;
-        x[a] = make_uint4(0u, 0u, 0u, 0u);
-        vm[a] = 0u;
-        if (v < vb) {
-          x[a] = reinterpret_cast<const uint4*>(sm)[v];
-          const int i0 = s.o + v * U;
-          vm[a] = (1u << U) - 1u;
-          if (i0 < s.lo) vm[a] &= ~0u << (s.lo - i0);
-          if (i0 + U > s.hi) vm[a] &= (1u << max(0, s.hi - i0)) - 1u;
-        }
-      }
-      vec(x[0], s.o + (v0 + (int)threadIdx.x) * U, vm[0], f);
-      if (v0 + kThreads < vb) vec(x[1], s.o + (v0 + kThreads + (int)threadIdx.x) * U, vm[1], f);
-    }
+  __device__ __forceinline__ void visit_range(int va, int vb, F&& f) const {
+    for (int v = va + (int)threadIdx.x; v < vb; v += kThreads)
+      vec(reinterpret_cast<const uint4*>(sm)[v], s.o + v * U, (1u << U) - 1u, f);
+  }
+
+  // The partial first and last vectors of the on-chip copy (threads 0 and 1).
+  template <class F>
+  __device__ __forceinline__ void visit_edges(F&& f) const {
+    const int head = s.vb0 ? 0 : -1;
+    const int tail = s.vb0 + s.nbv < s.nvec ? s.vb0 + s.nbv : -1;
+    const int v = threadIdx.x == 0 ? head : threadIdx.x == 1 ? tail : -1;
+    if (v < 0 || (threadIdx.x == 1 && tail == head)) return;
+    const int i0 = s.o + v * U;
+    unsigned vm = (1u << U) - 1u;
+    if (i0 < s.lo) vm &= ~0u << (s.lo - i0);
+    if (i0 + U > s.hi) vm &= (1u << max(0, s.hi - i0)) - 1u;
+    vec(reinterpret_cast<const uint4*>(sm)[v], i0, vm, f);
   }
 
   // Straight from global memory (slices too large to keep on chip).
@@ -159,69 +159,58 @@ struct SliceSrc {
   __device__ __forceinline__ void visit_global(F&& f) const {
     using E = Elt<DT>;
     const int nh = s.bl - s.lo, nt = s.hi - s.bh;
-    if ((threadIdx.x >> 5) == 0) {  // the unaligned head and tail, one element per lane
-      const int l = threadIdx.x & 31;
-      const bool v = l < nh + nt;
-      const int i = l < nh ? s.lo + l : s.bh + (l - nh);
+    if ((int)threadIdx.x < nh + nt) {  // the unaligned head and tail, one element per thread
+      const int i = (int)threadIdx.x < nh ? s.lo + (int)threadIdx.x : s.bh + ((int)threadIdx.x - nh);
       uint32_t key[U];
       int pos[U];
 #pragma unroll
       for (int j = 0; j < U; ++j) {
-        key[j] = E::key(v && j == 0 ? E::load(row, i) : 0u);
+        key[j] = E::key(j == 0 ? E::load(row, i) : 0u);
         pos[j] = i;
       }
-      f(key, pos, v ? 1u : 0u);
+      f(key, pos, 1u);
     }
     const uint4* body = reinterpret_cast<const uint4*>(row + (int64_t)s.bl * E::ES);
     const int nv = (s.bh - s.bl) / U;
     constexpr int kAhead = 4;
-    for (int v0 = 0; v0 < nv; v0 += kAhead * kThreads) {
+    for (int v0 = (int)threadIdx.x; v0 < nv; v0 += kAhead * kThreads) {
       uint4 x[kAhead];
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
-        const int v = v0 + a * kThreads + (int)threadIdx.x;
+        const int v = v0 + a * kThreads;
         x[a] = v < nv ? ld_nc_v4(body + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
-        const int v = v0 + a * kThreads + (int)threadIdx.x;
-        vec(x[a], s.bl + v * U, v < nv ? (1u << U) - 1u : 0u, f);
+        const int v = v0 + a * kThreads;
+        if (v < nv) vec(x[a], s.bl + v * U, (1u << U) - 1u, f);
       }
     }
   }
 
   template <class F>
   __device__ __forceinline__ void visit(F&& f) const {
-    if (s.resident)
-      visit_vecs(0, s.nvec, f);
-    else
+    if (s.resident) {
+      visit_range(s.vb0, s.vb0 + s.nbv, f);
+      visit_edges(f);
+    } else {
       visit_global(f);
+    }
   }
 };
 
-// (key, position) pairs in shared memory, four per lane per call.
+// (key, position) pairs in shared memory, one per call.
 struct CandSrc {
-  static constexpr int U = 4;
+  static constexpr int U = 1;
   const uint2* c;
   unsigned n;
   template <class F>
   __device__ __forceinline__ void visit(F&& f) const {
-    for (unsigned i0 = 0; i0 < n; i0 += U * kThreads) {
-      uint32_t key[U];
-      int pos[U];
-      unsigned vm = 0u;
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const unsigned i = i0 + j * kThreads + threadIdx.x;
-        uint2 e = make_uint2(0u, 0u);
-        if (i < n) {
-          e = c[i];
-          vm |= 1u << j;
-        }
-        key[j] = e.x;
-        pos[j] = (int)e.y;
-      }
-      f(key, pos, vm);
+    for (unsigned i = threadIdx.x; i < n; i += kThreads) {
+      const uint2 e = c[i];
+      const uint32_t key[1] = {e.x};
+      const int pos[1] = {(int)e.y};
+      f(key, pos, 1u);
     }
   }
 };
@@ -236,19 +225,13 @@ __device__ __forceinline__ void zero_counters(unsigned* h, int n) {
   for (int i = threadIdx.x; i < (n + 3) / 4; i += kThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Largest and smallest valid key of a lane's U elements (0 / ~0 if none).
+// Largest valid key of a group of U elements (0 if none).
 template <int U>
-__device__ __forceinline__ void key_range(const uint32_t (&key)[U], unsigned vm, uint32_t* mx,
-                                          uint32_t* mn) {
-  uint32_t a = 0u, b = ~0u;
+__device__ __forceinline__ uint32_t key_max(const uint32_t (&key)[U], unsigned vm) {
+  uint32_t a = 0u;
 #pragma unroll
-  for (int j = 0; j < U; ++j) {
-    const bool v = (vm >> j) & 1u;
-    a = max(a, v ? key[j] : 0u);
-    b = min(b, v ? key[j] : ~0u);
-  }
-  *mx = a;
-  *mn = b;
+  for (int j = 0; j < U; ++j) a = max(a, ((vm >> j) & 1u) ? key[j] : 0u);
+  return a;
 }
 
 // Histogram of digit D over the elements that match the prefix.
@@ -257,21 +240,12 @@ __device__ __forceinline__ void hist_round(const Src& src, unsigned* h, const Pr
                                            uint32_t pmax) {
   constexpr int U = Src::U;
   src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
-    // the value-key prefix is monotone in the key: skip vectors with no
-    // element inside it (one vote)
-    uint32_t mx, mn;
-    key_range<U>(key, vm, &mx, &mn);
-    const bool none = vm == 0u || (mx & P.kmask) < P.kpref || (mn & P.kmask) > P.kpref;
-    if (__all_sync(0xffffffffu, none)) return;
-    uint32_t d[U];
-    unsigned m = 0u;
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const uint32_t inv = pmax - (uint32_t)pos[j];
-      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0) m |= 1u << j;
-      d[j] = digit_value(D, key[j], inv);
+      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0)
+        atomicAdd(&h[digit_value(D, key[j], inv)], 1u);
     }
-    hist_add_vec<U>(h, d, m);
   });
 }
 
@@ -396,42 +370,29 @@ __device__ __forceinline__ void emit_round(const Src& src, const Prefix& P, Digi
   constexpr int U = Src::U;
   bool bad = false;
   // Every emitted element has (key & qmask) >= qval, and that part of the
-  // key is monotone in the key: vectors whose largest key fails it are
-  // skipped with one vote.
+  // key is monotone in the key: groups whose largest key fails it are skipped.
   uint32_t qmask = P.kmask, qval = P.kpref;
   if (!D.on_pos) {
     qmask |= ((1u << D.bits) - 1u) << D.shift;
     qval |= bin << D.shift;
   }
   src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
-    uint32_t mx, mn;
-    key_range<U>(key, vm, &mx, &mn);
-    if (__all_sync(0xffffffffu, vm == 0u || (mx & qmask) < qval)) return;
-    uint32_t d[U];
-    unsigned sel = 0u, to_cand = 0u;
+    if ((key_max<U>(key, vm) & qmask) < qval) return;  // nothing here reaches the threshold
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const uint32_t inv = pmax - (uint32_t)pos[j];
-      d[j] = digit_value(D, key[j], inv);
-      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], inv) == 0) {
-        if (d[j] > bin || (end == kEndFinal && d[j] == bin)) sel |= 1u << j;
-        if (end == kEndCollect && d[j] == bin) to_cand |= 1u << j;
-      }
-    }
-    sel |= to_cand;
-    if (!__any_sync(0xffffffffu, sel != 0u)) return;
-    unsigned o[U];
-    slots_vec<U>(offs, d, sel, o);
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      if (!((sel >> j) & 1u)) continue;
-      if ((to_cand >> j) & 1u) {
-        if (o[j] < cap)
-          put_cand(cand, o[j], key[j], pos[j], cand_global);
+      if (!((vm >> j) & 1u) || prefix_cmp(P, key[j], inv) != 0) continue;
+      const uint32_t d = digit_value(D, key[j], inv);
+      const bool to_cand = end == kEndCollect && d == bin;
+      if (!(d > bin || (end == kEndFinal && d == bin) || to_cand)) continue;
+      const unsigned o = atomicAdd(&offs[d], 1u);  // rank inside the bin, row-wide
+      if (to_cand) {
+        if (o < cap)
+          put_cand(cand, o, key[j], pos[j], cand_global);
         else
           bad = true;
       } else {
-        const unsigned slot = base + suf[d[j]] + o[j];
+        const unsigned slot = base + suf[d] + o;
         if (slot < k)
           out_row[slot] = pos[j];
         else
@@ -442,16 +403,25 @@ __device__ __forceinline__ void emit_round(const Src& src, const Prefix& P, Digi
   if (bad) atomicOr(status, kStatInternal);
 }
 
-// The highest still-varying bits (at most 12) of the composite key: value
-// key first, then the inverted position.  False when nothing varies.
-__device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, Digit* D) {
-  uint32_t& v = vk ? vk : vp;
+// The highest still-varying bits (at most `width`) of the composite key:
+// value key first, then the inverted position.  False when nothing varies.
+__device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, int width, Digit* D) {
+  const bool on_pos = vk == 0u;
+  uint32_t& v = on_pos ? vp : vk;
   if (!v) return false;
   const int hi = 31 - __clz((int)v);
-  const int lo = hi >= 11 ? hi - 11 : 0;
-  *D = {vk ? 0 : 1, lo, hi - lo + 1};
+  const int lo = hi >= width - 1 ? hi - (width - 1) : 0;
+  *D = {on_pos ? 1 : 0, lo, hi - lo + 1};
   v &= ~(((1u << (hi - lo + 1)) - 1u) << lo);
   return true;
+}
+
+// Digit width for a round over n elements: about two bins per element, so the
+// threshold bin usually ends up with one element (and the rounds end), while
+// small candidate sets get small, cheap histograms.
+__device__ __forceinline__ int digit_width(unsigned n) {
+  const int lg = 32 - __clz((int)max(n, 1u));  // ceil-ish log2(n) + 1
+  return min(kMaxDigitBits, max(4, lg + 1));
 }
 
 // Refines candidates held on chip until the k_rem wanted among them are
@@ -473,9 +443,10 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
   P.kpref |= and_k & ck;
   P.pmask |= cp;
   P.ppref |= and_i & cp;
+  unsigned live = n;  // elements matching the prefix
   for (;;) {
     Digit D;
-    if (!next_digit(vk, vp, &D)) {
+    if (!next_digit(vk, vp, digit_width(live), &D)) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
@@ -489,22 +460,16 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
     prefix_extend(P, D, bin);
     k_rem -= above;
     if (cnt == k_rem) break;
+    live = cnt;
   }
   if (threadIdx.x == 0) ctl->count = 0u;
   __syncthreads();
   bool bad = false;
   src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
-    unsigned sel = 0u;
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-      if (((vm >> j) & 1u) && prefix_cmp(P, key[j], pmax - (uint32_t)pos[j]) >= 0) sel |= 1u << j;
-    if (!__any_sync(0xffffffffu, sel != 0u)) return;
-    unsigned o[U];
-    ranks_vec<U>(&ctl->count, sel, o);
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      if (!((sel >> j) & 1u)) continue;
-      const unsigned slot = out_base + o[j];
+      if (!((vm >> j) & 1u) || prefix_cmp(P, key[j], pmax - (uint32_t)pos[j]) < 0) continue;
+      const unsigned slot = out_base + atomicAdd(&ctl->count, 1u);
       if (slot < k)
         out_row[slot] = pos[j];
       else
@@ -576,20 +541,20 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   s.bh = max(s.bl, (int)align_down((uint32_t)s.hi));
   s.o = s.lo < s.bl ? s.bl - (int)V : s.bl;
   s.nvec = (s.hi - s.o + (int)V - 1) / (int)V;
+  s.vb0 = s.lo < s.bl ? 1 : 0;
+  s.nbv = (s.bh - s.bl) / (int)V;
   s.resident = s.nvec * 16 <= kSliceBytes;
   const SliceSrc<DT> src{row, sl, s};
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
   constexpr int U = SliceSrc<DT>::U;
   auto f0 = [&](const uint32_t(&key)[U], const int(&)[U], unsigned vm) {
-    uint32_t d[U];
 #pragma unroll
-    for (int j = 0; j < U; ++j) d[j] = key[j] >> E::kShift0;
-    hist_add_vec<U>(h, d, vm);
+    for (int j = 0; j < U; ++j)
+      if ((vm >> j) & 1u) atomicAdd(&h[key[j] >> E::kShift0], 1u);
   };
   if (s.resident) {
-    const int vb0 = s.lo < s.bl ? 1 : 0;
-    const int nbv = (s.bh - s.bl) / (int)V;
+    const int vb0 = s.vb0, nbv = s.nbv;
     if (threadIdx.x == 0) {
       fence_proxy_async_smem();
       const unsigned long long pol = policy_evict_first();
@@ -610,14 +575,13 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       E::store(sl + (size_t)(i - s.o) * E::ES, E::load(row, i));
     }
     __syncthreads();
-    src.visit_vecs(0, vb0, f0);
-    src.visit_vecs(vb0 + nbv, s.nvec, f0);
+    src.visit_edges(f0);
     for (int c = 0; c < kChunks; ++c) {
       const int c0 = nbv * c / kChunks, c1 = nbv * (c + 1) / kChunks;
       if (c1 > c0) {
         mbar_wait_bounded(&ctl->mbar[c], (phase_bits >> c) & 1u, p.spin_limit_ns, ctl, status);
         phase_bits ^= 1u << c;
-        src.visit_vecs(vb0 + c0, vb0 + c1, f0);
+        src.visit_range(vb0 + c0, vb0 + c1, f0);
       }
     }
   } else {
@@ -715,18 +679,28 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
           const unsigned i = i0 + j * kThreads + threadIdx.x;
           e[j] = i < cnt ? ld_relaxed_u64(gc + i) : 0ull;
         }
+        // re-poll every still-empty word together until all have landed
+        for (;;) {
+          bool missing = false;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const unsigned i = i0 + j * kThreads + threadIdx.x;
+            if (i < cnt && e[j] == kCandEmpty) {
+              e[j] = ld_relaxed_u64(gc + i);
+              missing = true;
+            }
+          }
+          if (!missing) break;
+          if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+            ctl->ok = 0u;
+            atomicOr(status, kStatTimeout);
+            break;
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const unsigned i = i0 + j * kThreads + threadIdx.x;
           if (i >= cnt) continue;
-          while (e[j] == kCandEmpty) {
-            if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
-              ctl->ok = 0u;
-              atomicOr(status, kStatTimeout);
-              break;
-            }
-            e[j] = ld_relaxed_u64(gc + i);
-          }
           const uint2 c2 = make_uint2((uint32_t)e[j], (uint32_t)(e[j] >> 32));
           fc[i] = c2;
           gc[i] = kCandEmpty;
