@@ -45,8 +45,14 @@ struct SlotHdr {
   unsigned epoch;       // calls that used this slot so far
   unsigned used[2];     // digit rounds the last call of each parity used
   unsigned pad0;
-  unsigned arrive[2];   // barrier arrivals per parity, monotonic within a call
-  unsigned pad[10];
+  // Per parity: barrier arrivals (monotonic within a call) and, next to it so
+  // one 64-bit load reads both, 1 + the highest nonempty first-digit bin of
+  // the row (0 = none yet).
+  struct {
+    unsigned arrive;
+    unsigned top;
+  } sync[2];
+  unsigned pad[8];
 };
 static_assert(sizeof(SlotHdr) == 64, "slot header is one 64-byte line");
 constexpr size_t kSlotHistOff = sizeof(SlotHdr);
@@ -64,6 +70,7 @@ struct Ctl {
   unsigned warp32[kWarps + 1];
   unsigned pick_bin, pick_above, pick_cnt;
   unsigned ok;
+  unsigned top;
   unsigned count;
   unsigned red[4 * kWarps];
 };
@@ -260,6 +267,30 @@ __device__ __forceinline__ void note_pick(Ctl* ctl, unsigned bin, unsigned above
   }
 }
 
+// The same over bins [lo, hi) only, up to 4 bins per thread (hi - lo <=
+// 4 * kThreads); bins outside the range are neither read nor written.
+__device__ __forceinline__ void pick_and_suffix_range(unsigned* h, int lo, int hi, unsigned k_rem,
+                                                      Ctl* ctl) {
+  const int n = hi - lo;
+  const int per = (n + kThreads - 1) / kThreads;  // 0..4
+  const int b0 = lo + (int)threadIdx.x * per;
+  unsigned c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (i < per && b0 + i < hi) ? h[b0 + i] : 0u;
+  const unsigned s = c[0] + c[1] + c[2] + c[3];
+  unsigned total;
+  unsigned acc = block_suffix_excl(s, &total, ctl);
+#pragma unroll
+  for (int i = 3; i >= 0; --i) {
+    if (i < per && b0 + i < hi) {
+      note_pick(ctl, (unsigned)(b0 + i), acc, c[i], k_rem);
+      h[b0 + i] = acc;
+    }
+    acc += c[i];
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ void pick_and_suffix(unsigned* h, int nb, unsigned k_rem, Ctl* ctl) {
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
   if (nb >= kWarps * 128) {
@@ -312,23 +343,7 @@ __device__ __forceinline__ void pick_and_suffix(unsigned* h, int nb, unsigned k_
     return;
   }
   // Small digits: thread t owns `per` consecutive bins.
-  const int per = (nb + kThreads - 1) / kThreads;  // 1..3
-  const int b0 = threadIdx.x * per;
-  unsigned c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = (i < per && b0 + i < nb) ? h[b0 + i] : 0u;
-  const unsigned s = c[0] + c[1] + c[2] + c[3];
-  unsigned total;
-  unsigned acc = block_suffix_excl(s, &total, ctl);
-#pragma unroll
-  for (int i = 3; i >= 0; --i) {
-    if (i < per && b0 + i < nb) {
-      note_pick(ctl, (unsigned)(b0 + i), acc, c[i], k_rem);
-      h[b0 + i] = acc;
-    }
-    acc += c[i];
-  }
-  __syncthreads();
+  pick_and_suffix_range(h, 0, nb, k_rem, ctl);
 }
 
 // Block-wide OR and AND of per-thread partial results for two words
@@ -359,6 +374,65 @@ __device__ __forceinline__ void block_or_and(uint32_t& or_a, uint32_t& and_a, ui
     and_b &= ctl->red[4 * w + 3];
   }
   __syncthreads();
+}
+
+// From this block's first-digit counts h[0..kMaxBins) and each thread's
+// 1 + highest bin seen (top1): a lower bound for the threshold bin, namely
+// the start of the region (kMaxBins / (2 * kWarps) bins) holding the block's
+// k-th largest element (the row's k-th largest is at least as large; 0 if the
+// block holds fewer than k), and 1 + the block's highest nonempty bin.
+// One barrier.
+__device__ __forceinline__ void local_bounds(const unsigned* h, unsigned k, unsigned top1, Ctl* ctl,
+                                             int* floor_bin, unsigned* top) {
+  constexpr int kRegions = 2 * kWarps;
+  constexpr int kRegionBins = kMaxBins / kRegions;
+  constexpr int kVecPerLane = kRegionBins / 128;  // 16-byte vectors per lane and region
+  static_assert(kVecPerLane >= 1, "regions of at least 128 bins");
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) top1 = max(top1, __shfl_xor_sync(0xffffffffu, top1, off));
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int r = 2 * (int)warp + q;
+    const uint4* p = reinterpret_cast<const uint4*>(h + r * kRegionBins) + lane;
+    unsigned s = 0u;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      const uint4 v = p[32 * i];
+      s += v.x + v.y + v.z + v.w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) ctl->red[r] = s;
+  }
+  if (lane == 0) ctl->warp32[warp] = top1;
+  __syncthreads();
+  unsigned acc = 0u, t = 0u;
+  int fb = 0;
+  bool found = false;
+#pragma unroll
+  for (int r = kRegions - 1; r >= 0; --r) {
+    acc += ctl->red[r];
+    if (!found && acc >= k) {
+      fb = r * kRegionBins;
+      found = true;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t = max(t, ctl->warp32[w]);
+  __syncthreads();
+  *floor_bin = fb;
+  *top = t;
+}
+
+__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Candidate words in global memory, written and polled without caching.

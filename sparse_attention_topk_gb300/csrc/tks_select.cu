@@ -133,11 +133,25 @@ struct SliceSrc {
     f(key, pos, vm);
   }
 
-  // Whole vectors [va, vb) of the on-chip copy.
+  // Whole vectors [va, vb) of the on-chip copy, four loads in flight per
+  // thread (each iteration is otherwise one serial chain of latencies).
   template <class F>
   __device__ __forceinline__ void visit_range(int va, int vb, F&& f) const {
-    for (int v = va + (int)threadIdx.x; v < vb; v += kThreads)
-      vec(reinterpret_cast<const uint4*>(sm)[v], s.o + v * U, (1u << U) - 1u, f);
+    constexpr int B = 4;
+    const uint4* sv = reinterpret_cast<const uint4*>(sm);
+    for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads) {
+      uint4 x[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
+        x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
+        if (v < vb) vec(x[b], s.o + v * U, (1u << U) - 1u, f);
+      }
+    }
   }
 
   // The partial first and last vectors of the on-chip copy (threads 0 and 1).
@@ -199,18 +213,27 @@ struct SliceSrc {
   }
 };
 
-// (key, position) pairs in shared memory, one per call.
+// (key, position) pairs in shared memory, four per call (strided by the
+// block size, so the loads of a warp are contiguous).
 struct CandSrc {
-  static constexpr int U = 1;
+  static constexpr int U = 4;
   const uint2* c;
   unsigned n;
   template <class F>
   __device__ __forceinline__ void visit(F&& f) const {
-    for (unsigned i = threadIdx.x; i < n; i += kThreads) {
-      const uint2 e = c[i];
-      const uint32_t key[1] = {e.x};
-      const int pos[1] = {(int)e.y};
-      f(key, pos, 1u);
+    for (unsigned i0 = threadIdx.x; i0 < n; i0 += U * kThreads) {
+      uint32_t key[U];
+      int pos[U];
+      unsigned vm = 0u;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const unsigned i = i0 + j * kThreads;
+        const uint2 e = i < n ? c[i] : make_uint2(0u, 0u);
+        key[j] = e.x;
+        pos[j] = (int)e.y;
+        vm |= (i < n ? 1u : 0u) << j;
+      }
+      f(key, pos, vm);
     }
   }
 };
@@ -264,36 +287,46 @@ __device__ __forceinline__ void mbar_wait_bounded(unsigned long long* bar, unsig
   }
 }
 
-// Adds this block's counts into the row's L2 histogram.  The value each add
-// returns is this block's offset inside that bin across the row, kept in
-// offs[] to place the block's elements in the output later without any
-// further coordination.  Then a bounded barrier over the row's blocks, then
-// the row's summed counts replace the local ones in h[].
-__device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int nb, unsigned* g, unsigned* arrive,
-                            unsigned target, bool skip_arrive, long long limit, Ctl* ctl,
-                            unsigned* status) {
+// Adds this block's counts of bins [lo, hi) into the row's L2 histogram g.
+// The value each add returns is this block's offset inside that bin across
+// the row, kept in offs[] to place the block's elements in the output later
+// without any further coordination.  my_top (1 + this block's highest
+// nonempty bin, or 0) goes into the row's maximum.  Then a bounded barrier
+// over the row's blocks; after it the row's counts of bins [lo, top) replace
+// the local ones in h[], where top is the row's maximum (nb unless use_top).
+__device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int lo, int hi, int nb,
+                                            unsigned* g, unsigned* sync_pair, unsigned my_top,
+                                            bool use_top, unsigned target, bool skip_arrive,
+                                            long long limit, Ctl* ctl, unsigned* status) {
   constexpr int kPer = kMaxBins / kThreads;
   unsigned c[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
-    c[j] = b < nb ? h[b] : 0u;
+    c[j] = (b >= lo && b < hi) ? h[b] : 0u;
   }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
+  // the row maximum travels with the counts (an atomic with return, so it
+  // has been performed by the time the arrival below is released)
+  unsigned top_seen = 0u;
+  if (threadIdx.x == 0 && use_top && my_top) top_seen = atomicMax(&sync_pair[1], my_top);
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
-    if (b < nb) offs[b] = c[j];
+    if (b >= lo && b < hi) offs[b] = c[j];
   }
+  if (threadIdx.x == 0) ctl->top = top_seen;  // keeps the returned value live
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    if (!skip_arrive) atomicAdd(arrive, 1u);
+    // release: this block's adds (all returned before the barrier above) are
+    // visible to any block that sees the arrival
+    if (!skip_arrive) red_release_add_u32(&sync_pair[0], 1u);
     unsigned ok = 1u;
-    if (ld_acquire_u32(arrive) < target) {
+    unsigned long long w = ld_acquire_u64(sync_pair);
+    if ((unsigned)w < target) {
       const unsigned long long t0 = globaltimer_ns();
-      while (ld_acquire_u32(arrive) < target) {
+      while ((unsigned)(w = ld_acquire_u64(sync_pair)) < target) {
         if ((long long)(globaltimer_ns() - t0) > limit) {
           ok = 0u;
           atomicOr(status, kStatTimeout);
@@ -301,22 +334,49 @@ __device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int nb,
         }
       }
     }
-    __threadfence();
+    ctl->top = use_top ? min((unsigned)nb, (unsigned)(w >> 32)) : (unsigned)nb;
     ctl->ok = ok;
   }
   __syncthreads();
   if (!ctl->ok) return false;
+  const int top = (int)ctl->top;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
-    c[j] = b < nb ? __ldcg(g + b) : 0u;
+    c[j] = (b >= lo && b < top) ? __ldcg(g + b) : 0u;
   }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
-    if (b < nb) h[b] = c[j];
+    if (b >= lo && b < top) h[b] = c[j];
   }
   __syncthreads();
+  return true;
+}
+
+// Finds the threshold bin among bins [lo, hi) of h[0..nb) (the caller knows
+// it lies there) and turns those bins into exclusive suffix sums; false (and
+// an error) if the counts are inconsistent, which cannot happen unless memory
+// was corrupted.
+__device__ __forceinline__ bool pick_bin_range(unsigned* h, int lo, int hi, int nb, unsigned k_rem,
+                                               Ctl* ctl, unsigned* status, unsigned* bin,
+                                               unsigned* above, unsigned* cnt) {
+  if (threadIdx.x == 0) ctl->pick_bin = 0xFFFFFFFFu;
+  if (hi - lo <= 4 * kThreads) {
+    pick_and_suffix_range(h, lo, hi, k_rem, ctl);
+  } else {
+    for (int i = threadIdx.x; i < nb; i += kThreads)
+      if (i < lo || i >= hi) h[i] = 0u;
+    __syncthreads();
+    pick_and_suffix(h, nb, k_rem, ctl);
+  }
+  *bin = ctl->pick_bin;
+  *above = ctl->pick_above;
+  *cnt = ctl->pick_cnt;
+  if (*bin == 0xFFFFFFFFu) {
+    if (threadIdx.x == 0) atomicOr(status, kStatInternal);
+    return false;
+  }
   return true;
 }
 
@@ -410,7 +470,8 @@ __device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, int width
   uint32_t& v = on_pos ? vp : vk;
   if (!v) return false;
   const int hi = 31 - __clz((int)v);
-  const int lo = hi >= width - 1 ? hi - (width - 1) : 0;
+  const int lowest = __ffs((int)v) - 1;  // no digit reaches below the lowest varying bit
+  const int lo = max(lowest, hi >= width - 1 ? hi - (width - 1) : 0);
   *D = {on_pos ? 1 : 0, lo, hi - lo + 1};
   v &= ~(((1u << (hi - lo + 1)) - 1u) << lo);
   return true;
@@ -434,7 +495,6 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
                                uint32_t pmax, unsigned* h, int32_t* out_row, unsigned k, Ctl* ctl,
                                unsigned* status) {
   const CandSrc src{cand, n};
-  constexpr int U = CandSrc::U;
   const unsigned out_base = k - k_rem;
   uint32_t vk = (or_k ^ and_k) & ~P.kmask;
   uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
@@ -462,20 +522,161 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
     if (cnt == k_rem) break;
     live = cnt;
   }
-  if (threadIdx.x == 0) ctl->count = 0u;
-  __syncthreads();
-  bool bad = false;
-  src.visit([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+  // Write every candidate at or above the final prefix into consecutive
+  // slots: count per warp, scan over warps, then each warp writes its
+  // selected candidates in order (coalesced stores).
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  constexpr int B = 4;
+  const unsigned iters = (n + B * kThreads - 1) / (B * kThreads);
+  unsigned mine = 0u;
+  for (unsigned it = 0; it < iters; ++it) {
+    uint2 e[B];
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      if (!((vm >> j) & 1u) || prefix_cmp(P, key[j], pmax - (uint32_t)pos[j]) < 0) continue;
-      const unsigned slot = out_base + atomicAdd(&ctl->count, 1u);
+    for (int b = 0; b < B; ++b) {
+      const unsigned i = (it * B + b) * kThreads + threadIdx.x;
+      e[b] = i < n ? cand[i] : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const unsigned i = (it * B + b) * kThreads + threadIdx.x;
+      const bool sel = i < n && prefix_cmp(P, e[b].x, pmax - e[b].y) >= 0;
+      mine += (unsigned)__popc(__ballot_sync(0xffffffffu, sel));
+    }
+  }
+  if (lane == 0) ctl->warp32[warp] = mine;
+  __syncthreads();
+  unsigned wbase = out_base;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w)
+    if (w < (int)warp) wbase += ctl->warp32[w];
+  bool bad = false;
+  const unsigned lt = (1u << lane) - 1u;
+  for (unsigned it = 0; it < iters; ++it) {
+    uint2 e[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const unsigned i = (it * B + b) * kThreads + threadIdx.x;
+      e[b] = i < n ? cand[i] : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const unsigned i = (it * B + b) * kThreads + threadIdx.x;
+      const bool sel = i < n && prefix_cmp(P, e[b].x, pmax - e[b].y) >= 0;
+      const unsigned m = __ballot_sync(0xffffffffu, sel);
+      if (sel) {
+        const unsigned slot = wbase + (unsigned)__popc(m & lt);
+        if (slot < k)
+          out_row[slot] = (int)e[b].y;
+        else
+          bad = true;
+      }
+      wbase += (unsigned)__popc(m);
+    }
+  }
+  if (bad) atomicOr(status, kStatInternal);
+}
+
+// Candidates a thread keeps in registers in the register finisher.
+constexpr int kRegCand = 8;
+constexpr unsigned kRegCandCap = (unsigned)kRegCand * kThreads;
+
+// The finish for up to kRegCandCap candidates, held in registers: thread t
+// owns candidates t + j * kThreads (j < kRegCand) as (key, inverted
+// position) with an `alive` bit (still inside the prefix) and a `sel` bit
+// (known to be selected).  A digit round is then one predicated atomic per
+// alive candidate and a bit update, with no rereading and no prefix tests.
+// Writes the k_rem selected positions after the k - k_rem already emitted.
+__device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCand],
+                                                    const uint32_t (&ci)[kRegCand], unsigned alive,
+                                                    unsigned k_rem, Prefix P, uint32_t or_k,
+                                                    uint32_t and_k, uint32_t or_i, uint32_t and_i,
+                                                    unsigned n, uint32_t pmax, unsigned* h,
+                                                    int32_t* out_row, unsigned k, Ctl* ctl,
+                                                    unsigned* status) {
+  const unsigned out_base = k - k_rem;
+  uint32_t vk = (or_k ^ and_k) & ~P.kmask;
+  uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
+  unsigned sel = 0u;
+  unsigned live = n;
+  for (;;) {
+    Digit D;
+    if (!next_digit(vk, vp, digit_width(live), &D)) {
+      if (threadIdx.x == 0) atomicOr(status, kStatInternal);
+      return;
+    }
+    const int nb = 1 << D.bits;
+    zero_counters(h, nb);
+    __syncthreads();
+    uint32_t d[kRegCand];
+#pragma unroll
+    for (int j = 0; j < kRegCand; ++j) {
+      d[j] = digit_value(D, ck[j], ci[j]);
+      if ((alive >> j) & 1u) atomicAdd(&h[d[j]], 1u);
+    }
+    __syncthreads();
+    unsigned bin, above, cnt;
+    if (!pick_bin(h, nb, k_rem, ctl, status, &bin, &above, &cnt)) return;
+#pragma unroll
+    for (int j = 0; j < kRegCand; ++j) {
+      if (!((alive >> j) & 1u)) continue;
+      if (d[j] > bin) sel |= 1u << j;
+      if (d[j] != bin) alive &= ~(1u << j);
+    }
+    k_rem -= above;
+    if (cnt == k_rem) {
+      sel |= alive;
+      break;
+    }
+    live = cnt;
+  }
+  unsigned total;
+  unsigned slot = out_base + block_suffix_excl((unsigned)__popc(sel), &total, ctl);
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kRegCand; ++j) {
+    if (!((sel >> j) & 1u)) continue;
+    if (slot < k)
+      out_row[slot] = (int)(pmax - ci[j]);
+    else
+      bad = true;
+    ++slot;
+  }
+  if (bad) atomicOr(status, kStatInternal);
+}
+
+// The same emission as emit_round for the (at most two) elements a thread
+// tracked during round 0: (k1, p1) and (k2, p2), position -1 when absent.
+__device__ __forceinline__ void emit_tracked(uint32_t k1, int p1, uint32_t k2, int p2,
+                                             const Prefix& P, Digit D, unsigned bin, int end,
+                                             unsigned base, const unsigned* suf, unsigned* offs,
+                                             uint32_t pmax, int32_t* out_row, unsigned k,
+                                             uint2* cand, bool cand_global, unsigned cap,
+                                             unsigned* status) {
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const uint32_t key = e == 0 ? k1 : k2;
+    const int pos = e == 0 ? p1 : p2;
+    if (pos < 0) continue;
+    const uint32_t inv = pmax - (uint32_t)pos;
+    if (prefix_cmp(P, key, inv) != 0) continue;
+    const uint32_t d = digit_value(D, key, inv);
+    const bool to_cand = end == kEndCollect && d == bin;
+    if (!(d > bin || (end == kEndFinal && d == bin) || to_cand)) continue;
+    const unsigned o = atomicAdd(&offs[d], 1u);
+    if (to_cand) {
+      if (o < cap)
+        put_cand(cand, o, key, pos, cand_global);
+      else
+        bad = true;
+    } else {
+      const unsigned slot = base + suf[d] + o;
       if (slot < k)
-        out_row[slot] = pos[j];
+        out_row[slot] = pos;
       else
         bad = true;
     }
-  });
+  }
   if (bad) atomicOr(status, kStatInternal);
 }
 
@@ -548,10 +749,14 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
   constexpr int U = SliceSrc<DT>::U;
+  unsigned top1 = 0u;  // 1 + highest first-digit bin this thread saw
   auto f0 = [&](const uint32_t(&key)[U], const int(&)[U], unsigned vm) {
 #pragma unroll
     for (int j = 0; j < U; ++j)
-      if ((vm >> j) & 1u) atomicAdd(&h[key[j] >> E::kShift0], 1u);
+      if ((vm >> j) & 1u) {
+        atomicAdd(&h[key[j] >> E::kShift0], 1u);
+        top1 = max(top1, (key[j] >> E::kShift0) + 1u);
+      }
   };
   if (s.resident) {
     const int vb0 = s.vb0, nbv = s.nbv;
@@ -590,6 +795,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   }
   __syncthreads();
   if (!ctl->ok) return false;
+  // Bins the first threshold can lie in: from this block's own lower bound
+  // up to its highest nonempty bin (and, after the merge, the row's).
+  int floor0;
+  unsigned top0;
+  local_bounds(h, k, top1, ctl, &floor0, &top0);
 
   // Counters of this call's parity; the other parity's are cleared below.
   const unsigned epoch = hdr.x, par = epoch & 1u;
@@ -622,18 +832,24 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       hist_round(src, h, P, D, pmax);
       __syncthreads();
     }
+    int lo = 0, hi = nb;
+    if (t == 0) {
+      lo = floor0;
+      hi = (int)top0;
+    }
     if (group > 1) {
       const bool skip = p.test_skip_arrive && part == 0 && t == 0;
-      if (!group_merge(h, offs, nb, slot_hist + (size_t)t * kMaxBins, &slot->arrive[par],
-                       (unsigned)group * (t + 1), skip, p.spin_limit_ns, ctl, status))
+      if (!group_merge(h, offs, lo, hi, nb, slot_hist + (size_t)t * kMaxBins, &slot->sync[par].arrive,
+                       top0, t == 0, (unsigned)group * (t + 1), skip, p.spin_limit_ns, ctl, status))
         return false;
+      hi = (int)ctl->top;
       // every block of the call has read the epoch: the next call may use the other set
       if (t == 0 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
     } else {
       zero_counters(offs, nb);
     }
     unsigned bin, above;
-    if (!pick_bin(h, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
+    if (!pick_bin_range(h, lo, hi, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
     const unsigned need = k_rem - above;
     end = cnt == need ? kEndFinal : cnt <= cap ? kEndCollect : kEndAbove;
     emit_round(src, P, D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
@@ -649,7 +865,26 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   }
 
   if (group == 1) {
-    if (end == kEndCollect) {
+    if (end == kEndCollect && cnt <= kRegCandCap) {
+      __syncthreads();
+      uint32_t ck[kRegCand], ci[kRegCand];
+      unsigned alive = 0u;
+      uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
+#pragma unroll
+      for (int j = 0; j < kRegCand; ++j) {
+        const unsigned i = j * kThreads + threadIdx.x;
+        const uint2 c = i < cnt ? lcand[i] : make_uint2(0u, 0u);
+        ck[j] = c.x;
+        ci[j] = pmax - c.y;
+        if (i < cnt) {
+          alive |= 1u << j;
+          ok_ |= ck[j]; ak &= ck[j]; oi |= ci[j]; ai &= ci[j];
+        }
+      }
+      block_or_and(ok_, ak, oi, ai, ctl);
+      finish_in_registers(ck, ci, alive, k_rem, P, ok_, ak, oi, ai, cnt, pmax, h, out_row, k, ctl,
+                          status);
+    } else if (end == kEndCollect) {
       __syncthreads();
       uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
       for (unsigned i = threadIdx.x; i < cnt; i += kThreads) {
@@ -665,7 +900,54 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
 
   // ---- rows split over blocks ----
   if (part == 0) {
-    if (end == kEndCollect) {
+    if (end == kEndCollect && cnt <= kRegCandCap) {
+      // Gather the row's candidates straight into registers as they land
+      // (each word starts as all ones), put the words back to all ones for
+      // the next call, then finish in registers.
+      unsigned long long* gc = reinterpret_cast<unsigned long long*>(slot_cand);
+      unsigned long long e[kRegCand];
+#pragma unroll
+      for (int j = 0; j < kRegCand; ++j) {
+        const unsigned i = j * kThreads + threadIdx.x;
+        e[j] = i < cnt ? ld_relaxed_u64(gc + i) : 0ull;
+      }
+      const unsigned long long t0 = globaltimer_ns();
+      for (;;) {
+        bool missing = false;
+#pragma unroll
+        for (int j = 0; j < kRegCand; ++j) {
+          const unsigned i = j * kThreads + threadIdx.x;
+          if (i < cnt && e[j] == kCandEmpty) {
+            e[j] = ld_relaxed_u64(gc + i);
+            missing = true;
+          }
+        }
+        if (!missing) break;
+        if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+          ctl->ok = 0u;
+          atomicOr(status, kStatTimeout);
+          break;
+        }
+      }
+      uint32_t ck[kRegCand], ci[kRegCand];
+      unsigned alive = 0u;
+      uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
+#pragma unroll
+      for (int j = 0; j < kRegCand; ++j) {
+        const unsigned i = j * kThreads + threadIdx.x;
+        ck[j] = (uint32_t)e[j];
+        ci[j] = pmax - (uint32_t)(e[j] >> 32);
+        if (i < cnt) {
+          gc[i] = kCandEmpty;
+          alive |= 1u << j;
+          ok_ |= ck[j]; ak &= ck[j]; oi |= ci[j]; ai &= ci[j];
+        }
+      }
+      block_or_and(ok_, ak, oi, ai, ctl);
+      if (!ctl->ok) return false;
+      finish_in_registers(ck, ci, alive, k_rem, P, ok_, ak, oi, ai, cnt, pmax, h, out_row, k, ctl,
+                          status);
+    } else if (end == kEndCollect) {
       // Gather the row's candidates as they land (each slot starts as all
       // ones), put the slots back to all ones for the next call, then finish.
       uint2* fc = reinterpret_cast<uint2*>(sl);  // this block's slice copy is no longer needed
@@ -724,7 +1006,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     const unsigned w0 = min(words, me * per), w1 = min(words, w0 + per);
     for (unsigned i = w0 / 4 + threadIdx.x; i < w1 / 4; i += kThreads)
       reinterpret_cast<uint4*>(other)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (me == 0 && threadIdx.x == 0) slot->arrive[par ^ 1u] = 0u;
+    if (me == 0 && threadIdx.x == 0) {
+      slot->sync[par ^ 1u].arrive = 0u;
+      slot->sync[par ^ 1u].top = 0u;
+    }
   }
   return true;
 }
