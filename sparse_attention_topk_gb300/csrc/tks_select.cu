@@ -644,42 +644,6 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   if (bad) atomicOr(status, kStatInternal);
 }
 
-// The same emission as emit_round for the (at most two) elements a thread
-// tracked during round 0: (k1, p1) and (k2, p2), position -1 when absent.
-__device__ __forceinline__ void emit_tracked(uint32_t k1, int p1, uint32_t k2, int p2,
-                                             const Prefix& P, Digit D, unsigned bin, int end,
-                                             unsigned base, const unsigned* suf, unsigned* offs,
-                                             uint32_t pmax, int32_t* out_row, unsigned k,
-                                             uint2* cand, bool cand_global, unsigned cap,
-                                             unsigned* status) {
-  bool bad = false;
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const uint32_t key = e == 0 ? k1 : k2;
-    const int pos = e == 0 ? p1 : p2;
-    if (pos < 0) continue;
-    const uint32_t inv = pmax - (uint32_t)pos;
-    if (prefix_cmp(P, key, inv) != 0) continue;
-    const uint32_t d = digit_value(D, key, inv);
-    const bool to_cand = end == kEndCollect && d == bin;
-    if (!(d > bin || (end == kEndFinal && d == bin) || to_cand)) continue;
-    const unsigned o = atomicAdd(&offs[d], 1u);
-    if (to_cand) {
-      if (o < cap)
-        put_cand(cand, o, key, pos, cand_global);
-      else
-        bad = true;
-    } else {
-      const unsigned slot = base + suf[d] + o;
-      if (slot < k)
-        out_row[slot] = pos;
-      else
-        bad = true;
-    }
-  }
-  if (bad) atomicOr(status, kStatInternal);
-}
-
 // Selects the top k of row r with this block as part `part` of `group`.
 // Returns false after an unrecoverable device-side error.
 template <int DT>
