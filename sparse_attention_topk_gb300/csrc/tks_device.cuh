@@ -13,7 +13,10 @@ namespace tks {
 // 256 threads per block, one block per SM.  Control steps (scans, threshold
 // search, bookkeeping) are issued once per warp, so fewer warps make them
 // faster; the streaming steps are bound by data, not by the warp count.
-constexpr int kThreads = 256;
+#ifndef TKS_THREADS
+#define TKS_THREADS 256
+#endif
+constexpr int kThreads = TKS_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDigitBits = 12;            // widest digit: 4096 bins (16 KiB of counters)
 constexpr int kMaxBins = 1 << kMaxDigitBits;
@@ -378,22 +381,20 @@ __device__ __forceinline__ void block_or_and(uint32_t& or_a, uint32_t& and_a, ui
 
 // From this block's first-digit counts h[0..kMaxBins) and each thread's
 // 1 + highest bin seen (top1): a lower bound for the threshold bin, namely
-// the start of the region (kMaxBins / (2 * kWarps) bins) holding the block's
+// the start of the region (kMaxBins / 16 bins) holding the block's
 // k-th largest element (the row's k-th largest is at least as large; 0 if the
 // block holds fewer than k), and 1 + the block's highest nonempty bin.
 // One barrier.
 __device__ __forceinline__ void local_bounds(const unsigned* h, unsigned k, unsigned top1, Ctl* ctl,
                                              int* floor_bin, unsigned* top) {
-  constexpr int kRegions = 2 * kWarps;
+  constexpr int kRegions = 16;
   constexpr int kRegionBins = kMaxBins / kRegions;
   constexpr int kVecPerLane = kRegionBins / 128;  // 16-byte vectors per lane and region
-  static_assert(kVecPerLane >= 1, "regions of at least 128 bins");
+  static_assert(kVecPerLane >= 1 && kRegions <= 4 * kWarps, "region layout");
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) top1 = max(top1, __shfl_xor_sync(0xffffffffu, top1, off));
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int r = 2 * (int)warp + q;
+  for (int r = (int)warp; r < kRegions; r += kWarps) {
     const uint4* p = reinterpret_cast<const uint4*>(h + r * kRegionBins) + lane;
     unsigned s = 0u;
 #pragma unroll

@@ -580,15 +580,57 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
 constexpr int kRegCand = 8;
 constexpr unsigned kRegCandCap = (unsigned)kRegCand * kThreads;
 
+// A digit over the composite key (value key, inverted position) that may
+// span both fields: kb value-key bits from bit klo, then pb position bits
+// from bit plo (position bits only once no value-key bit below the digit
+// still varies, so digit order stays the composite order).
+struct Digit2 {
+  int klo, kb, plo, pb;
+};
+
+__device__ __forceinline__ bool next_digit2(uint32_t& vk, uint32_t& vp, int width, Digit2* D) {
+  D->kb = 0;
+  D->pb = 0;
+  D->klo = 0;
+  D->plo = 0;
+  int w = width;
+  if (vk) {
+    const int hi = 31 - __clz((int)vk);
+    const int lo = max(__ffs((int)vk) - 1, hi - (w - 1));
+    D->klo = lo;
+    D->kb = hi - lo + 1;
+    vk &= ~(((1u << D->kb) - 1u) << lo);
+    w -= D->kb;
+    if (vk) return true;  // lower value-key bits still vary: no position bits yet
+  }
+  if (w > 0 && vp) {
+    const int hi = 31 - __clz((int)vp);
+    const int lo = max(__ffs((int)vp) - 1, hi - (w - 1));
+    D->plo = lo;
+    D->pb = hi - lo + 1;
+    vp &= ~(((1u << D->pb) - 1u) << lo);
+  }
+  return D->kb + D->pb > 0;
+}
+
+__device__ __forceinline__ uint32_t digit2_value(const Digit2& D, uint32_t key, uint32_t inv) {
+  const uint32_t kpart = (key >> D.klo) & ((1u << D.kb) - 1u);
+  const uint32_t ppart = (inv >> D.plo) & ((1u << D.pb) - 1u);
+  return (kpart << D.pb) | ppart;
+}
+
 // The finish for up to kRegCandCap candidates, held in registers: thread t
 // owns candidates t + j * kThreads (j < kRegCand) as (key, inverted
 // position) with an `alive` bit (still inside the prefix) and a `sel` bit
 // (known to be selected).  A digit round is then one predicated atomic per
 // alive candidate and a bit update, with no rereading and no prefix tests.
-// Writes the k_rem selected positions after the k - k_rem already emitted.
+// Digits cover only bits that differ among the candidates and may run from
+// the value key into the position, so ties are usually broken in the same
+// round.  Writes the k_rem selected positions after the k - k_rem already
+// emitted.
 __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCand],
                                                     const uint32_t (&ci)[kRegCand], unsigned alive,
-                                                    unsigned k_rem, Prefix P, uint32_t or_k,
+                                                    unsigned k_rem, const Prefix& P, uint32_t or_k,
                                                     uint32_t and_k, uint32_t or_i, uint32_t and_i,
                                                     unsigned n, uint32_t pmax, unsigned* h,
                                                     int32_t* out_row, unsigned k, Ctl* ctl,
@@ -599,18 +641,18 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   unsigned sel = 0u;
   unsigned live = n;
   for (;;) {
-    Digit D;
-    if (!next_digit(vk, vp, digit_width(live), &D)) {
+    Digit2 D;
+    if (!next_digit2(vk, vp, digit_width(live), &D)) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
-    const int nb = 1 << D.bits;
+    const int nb = 1 << (D.kb + D.pb);
     zero_counters(h, nb);
     __syncthreads();
     uint32_t d[kRegCand];
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
-      d[j] = digit_value(D, ck[j], ci[j]);
+      d[j] = digit2_value(D, ck[j], ci[j]);
       if ((alive >> j) & 1u) atomicAdd(&h[d[j]], 1u);
     }
     __syncthreads();
