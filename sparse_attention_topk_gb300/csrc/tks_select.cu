@@ -858,7 +858,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (!pick_bin_range(h, lo, hi, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
     const unsigned need = k_rem - above;
     end = cnt == need ? kEndFinal : cnt <= cap ? kEndCollect : kEndAbove;
-    emit_round(src, P, D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
+    // (a round that only passes the threshold on, with nothing above its bin
+    // anywhere in the row, has nothing to emit)
+    if (end != kEndAbove || above != 0u)
+      emit_round(src, P, D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
     prefix_extend(P, D, bin);
     base += above;
     k_rem = need;
