@@ -83,6 +83,11 @@ typedef enum {
  * and never synchronise, so they can be captured.  Calls on one stream run in
  * order; calls on different streams use different workspaces.
  *
+ * Scheduling: the kernel is launched with programmatic stream serialisation,
+ * so it may be made resident while the previous kernel of the stream is still
+ * finishing; it waits for that kernel to complete (and for its writes to be
+ * visible) before it reads or writes any global memory.
+ *
  * Errors: argument errors return TKS_E_INVAL and launch nothing; CUDA errors
  * during setup or launch return TKS_E_CUDA.  Errors detected on the device
  * are recorded in the stream's workspace; read them with tks_device_status().
@@ -115,8 +120,11 @@ int tks_release(void);
  *                            value, clamped to what the device can co-schedule
  *   TKS_OPT_SPIN_LIMIT_NS    how long a block waits for the others of its row
  *                            before giving up with TKS_E_TIMEOUT (default 1 s)
- *   TKS_OPT_MIN_PER_BLOCK    automatic split: at least this many elements per
- *                            block (default chosen by measurement)
+ *   TKS_OPT_MIN_PER_BLOCK    automatic split: rows of at most 4096 elements
+ *                            stay on one block; longer rows get one block per
+ *                            this many elements (default 2048, chosen by
+ *                            measurement), leaving one block slot of the
+ *                            device free when the row count allows
  *   TKS_OPT_TEST_SKIP_ARRIVE test only: 1 makes the first block of each row
  *                            skip its first arrival, so the others' waits run
  *                            out and report TKS_E_TIMEOUT; 0 = off

@@ -1027,10 +1027,17 @@ template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
+  // The next kernel of the stream may be scheduled as soon as SMs free up;
+  // it waits below before touching memory, so this one runs ahead too.
+  grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int c = 0; c < kChunks; ++c) mbar_init(&ctl->mbar[c], 1u);
     fence_mbar_init();
   }
+  // Everything before this point is on-chip; the kernel ahead in the stream
+  // (its writes to the inputs, the outputs and the workspace included) is
+  // complete after it.
+  grid_dependency_wait();
   __syncthreads();
   unsigned phase_bits = 0u;
   if (p.group > 1) {
@@ -1065,7 +1072,8 @@ std::map<std::pair<int, void*>, Workspace> g_ws;
 
 std::atomic<long long> g_force_group{0};
 std::atomic<long long> g_spin_limit_ns{1000000000LL};
-std::atomic<long long> g_min_per_block{4096};
+std::atomic<long long> g_min_per_block{2048};
+constexpr long long kLoneRowMax = 4096;  // rows this short are never split
 std::atomic<long long> g_test_skip_arrive{0};
 
 int device_info(int dev, DeviceInfo* out) {
@@ -1111,14 +1119,20 @@ void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* gr
     *grid = cap;
     return;
   }
-  const int per = cap / batch;
+  // Rows split over blocks leave one block slot of the device free when they
+  // can, so that the blocks of the next call are all resident by the time the
+  // finishing block of this one is done.
+  const int per = (cap > 1 ? cap - 1 : cap) / batch;
   long long g;
   const long long forced = g_force_group.load();
   if (forced > 0) {
     g = forced;
   } else {
+    // short rows stay on one block (a split costs a round trip through L2
+    // that a block of their size does not make up for); longer ones get a
+    // block per g_min_per_block elements
     const long long mpb = g_min_per_block.load() > 0 ? g_min_per_block.load() : 1;
-    g = (row_stride + mpb - 1) / mpb;
+    g = row_stride <= kLoneRowMax ? 1 : (row_stride + mpb - 1) / mpb;
   }
   if (g > per) g = per;
   if (g < 1) g = 1;
@@ -1170,6 +1184,25 @@ int get_workspace(int dev, void* stream, const DeviceInfo& d, Workspace* out) {
 
 using namespace tks;
 
+// Launch attributes: programmatic stream serialisation (the kernel may be
+// scheduled while the previous kernel of the stream finishes; it waits for it
+// before its first memory access), and a cooperative launch when the blocks of
+// a row wait for one another, so that they are all resident.
+static void set_launch_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int group) {
+  std::memset(attr, 0, 2 * sizeof(cudaLaunchAttribute));
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (group > 1) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg->attrs = attr;
+  cfg->numAttrs = (unsigned)n;
+}
+
 extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int32_t batch,
                                 int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
                                 void* stream) {
@@ -1219,15 +1252,8 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
-  std::memset(attr, 0, sizeof attr);
-  if (group > 1) {
-    // blocks of a row wait for one another: they must all be resident
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  cudaLaunchAttribute attr[2];
+  set_launch_attrs(&cfg, attr, group);
   cudaError_t e = dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0>, p)
                                    : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
   if (e != cudaSuccess) {
@@ -1308,7 +1334,7 @@ extern "C" int tks_set_option(int option, int64_t value) {
   switch (option) {
     case TKS_OPT_FORCE_GROUP: g_force_group.store(value); return TKS_OK;
     case TKS_OPT_SPIN_LIMIT_NS: g_spin_limit_ns.store(value > 0 ? value : 1); return TKS_OK;
-    case TKS_OPT_MIN_PER_BLOCK: g_min_per_block.store(value > 0 ? value : 4096); return TKS_OK;
+    case TKS_OPT_MIN_PER_BLOCK: g_min_per_block.store(value > 0 ? value : 2048); return TKS_OK;
     case TKS_OPT_TEST_SKIP_ARRIVE: g_test_skip_arrive.store(value ? 1 : 0); return TKS_OK;
     default: return TKS_E_INVAL;
   }
@@ -1422,14 +1448,8 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  std::memset(attr, 0, sizeof attr);
-  if (group > 1) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  cudaLaunchAttribute attr[2];
+  set_launch_attrs(&cfg, attr, group);
   const cudaError_t e = dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0>, p)
                                          : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
   if (e != cudaSuccess) {
