@@ -78,6 +78,8 @@ struct Ctl {
   unsigned ok;
   unsigned top;
   unsigned qn;                 // marked steps queued for a pass
+  unsigned lo;                 // first-round floor bin of this block
+  unsigned sink;               // keeps an atomic's returned value live
   unsigned red[4 * kWarps];
   unsigned queue[kQueueCap];   // first vector of each marked step
 };
@@ -391,53 +393,6 @@ __device__ __forceinline__ void block_or_and(uint32_t& or_a, uint32_t& and_a, ui
     and_b &= ctl->red[4 * w + 3];
   }
   __syncthreads();
-}
-
-// From this block's first-digit counts h[0..kMaxBins) and each thread's
-// 1 + highest bin seen (top1): a lower bound for the threshold bin, namely
-// the start of the region (kMaxBins / 16 bins) holding the block's
-// k-th largest element (the row's k-th largest is at least as large; 0 if the
-// block holds fewer than k), and 1 + the block's highest nonempty bin.
-// One barrier.
-__device__ __forceinline__ void local_bounds(const unsigned* h, unsigned k, unsigned top1, Ctl* ctl,
-                                             int* floor_bin, unsigned* top) {
-  constexpr int kRegions = 16;
-  constexpr int kRegionBins = kMaxBins / kRegions;
-  constexpr int kVecPerLane = kRegionBins / 128;  // 16-byte vectors per lane and region
-  static_assert(kVecPerLane >= 1 && kRegions <= 4 * kWarps, "region layout");
-  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) top1 = max(top1, __shfl_xor_sync(0xffffffffu, top1, off));
-  for (int r = (int)warp; r < kRegions; r += kWarps) {
-    const uint4* p = reinterpret_cast<const uint4*>(h + r * kRegionBins) + lane;
-    unsigned s = 0u;
-#pragma unroll
-    for (int i = 0; i < kVecPerLane; ++i) {
-      const uint4 v = p[32 * i];
-      s += v.x + v.y + v.z + v.w;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) ctl->red[r] = s;
-  }
-  if (lane == 0) ctl->warp32[warp] = top1;
-  __syncthreads();
-  unsigned acc = 0u, t = 0u;
-  int fb = 0;
-  bool found = false;
-#pragma unroll
-  for (int r = kRegions - 1; r >= 0; --r) {
-    acc += ctl->red[r];
-    if (!found && acc >= k) {
-      fb = r * kRegionBins;
-      found = true;
-    }
-  }
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t = max(t, ctl->warp32[w]);
-  __syncthreads();
-  *floor_bin = fb;
-  *top = t;
 }
 
 __device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {

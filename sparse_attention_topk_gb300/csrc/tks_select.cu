@@ -382,40 +382,18 @@ __device__ __forceinline__ void mbar_wait_bounded(unsigned long long* bar, unsig
   }
 }
 
-// Adds this block's counts of bins [lo, hi) into the row's L2 histogram g.
-// The value each add returns is this block's offset inside that bin across
-// the row, kept in offs[] to place the block's elements in the output later
-// without any further coordination.  my_top (1 + this block's highest
-// nonempty bin, or 0) goes into the row's maximum.  Then a bounded barrier
-// over the row's blocks; after it the row's counts of bins [lo, top) replace
-// the local ones in h[], where top is the row's maximum (nb unless use_top).
-__device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int lo, int hi, int nb,
-                                            unsigned* g, unsigned* sync_pair, unsigned my_top,
-                                            bool use_top, unsigned target, bool skip_arrive,
-                                            long long limit, Ctl* ctl, unsigned* status) {
+// The row barrier after a merge, then the row's counts of bins [lo, top)
+// replace the local ones in h[].  top is the row's maximum (from the word
+// beside the arrival count) when use_top, else nb; it is left in ctl->top.
+// Bounded: on time-out records the error and returns false.
+__device__ __forceinline__ bool merge_wait_load(unsigned* h, int lo, int nb, const unsigned* g,
+                                                unsigned* sync_pair, bool use_top, unsigned target,
+                                                bool skip_arrive, long long limit, Ctl* ctl,
+                                                unsigned* status) {
   constexpr int kPer = kMaxBins / kThreads;
-  unsigned c[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    c[j] = (b >= lo && b < hi) ? h[b] : 0u;
-  }
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
-  // the row maximum travels with the counts (an atomic with return, so it
-  // has been performed by the time the arrival below is released)
-  unsigned top_seen = 0u;
-  if (threadIdx.x == 0 && use_top && my_top) top_seen = atomicMax(&sync_pair[1], my_top);
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    if (b >= lo && b < hi) offs[b] = c[j];
-  }
-  if (threadIdx.x == 0) ctl->top = top_seen;  // keeps the returned value live
-  __syncthreads();
   if (threadIdx.x == 0) {
-    // release: this block's adds (all returned before the barrier above) are
-    // visible to any block that sees the arrival
+    // release: this block's adds (all returned before the caller's barrier)
+    // are visible to any block that sees the arrival
     if (!skip_arrive) red_release_add_u32(&sync_pair[0], 1u);
     unsigned ok = 1u;
     unsigned long long w = ld_acquire_u64(sync_pair);
@@ -435,6 +413,7 @@ __device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int lo,
   __syncthreads();
   if (!ctl->ok) return false;
   const int top = (int)ctl->top;
+  unsigned c[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
@@ -446,6 +425,112 @@ __device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int lo,
     if (b >= lo && b < top) h[b] = c[j];
   }
   __syncthreads();
+  return true;
+}
+
+// Adds this block's counts of all nb bins into the row's L2 histogram g
+// (rounds after the first).  The value each add returns is this block's
+// offset inside that bin across the row, kept in offs[] to place the block's
+// elements in the output later without any further coordination.  Then the
+// row barrier and the row's counts in h[0, nb).
+__device__ __forceinline__ bool group_merge(unsigned* h, unsigned* offs, int nb, unsigned* g,
+                                            unsigned* sync_pair, unsigned target, long long limit,
+                                            Ctl* ctl, unsigned* status) {
+  constexpr int kPer = kMaxBins / kThreads;
+  unsigned c[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    c[j] = b < nb ? h[b] : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    if (b < nb) offs[b] = c[j];
+  }
+  __syncthreads();
+  return merge_wait_load(h, 0, nb, g, sync_pair, false, target, false, limit, ctl, status);
+}
+
+// Round 0: this block's bounds and, for a row split over blocks, the merge.
+// A bin can hold the row's threshold only if fewer than k of this block's
+// elements lie above it (the row's k-th largest is at least this block's k-th
+// largest): the lowest such bin is the block's floor, *lo.  *hi is 1 + the
+// highest nonempty bin, of the row when split, else of the block.  Both come
+// from one block-wide scan over per-thread sums of kPer consecutive bins.
+// When split, the block's counts of bins [*lo, block top) go into the row's
+// L2 histogram g (warp-wide adds over consecutive bins; the value each add
+// returns is this block's offset inside the bin, kept in offs[]), the block
+// top into the word beside the arrival count, and after the row barrier
+// h[*lo, *hi) holds the row's counts.
+__device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs, unsigned k,
+                                                    bool split, unsigned* g, unsigned* sync_pair,
+                                                    unsigned target, bool skip_arrive,
+                                                    long long limit, Ctl* ctl, unsigned* status,
+                                                    int* lo, int* hi) {
+  constexpr int kPer = kMaxBins / kThreads;
+  static_assert(kPer % 4 == 0, "bins per thread");
+  const int b0 = (int)threadIdx.x * kPer;
+  unsigned c[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer / 4; ++q) {
+    const uint4 v = reinterpret_cast<const uint4*>(h + b0)[q];
+    c[4 * q] = v.x;
+    c[4 * q + 1] = v.y;
+    c[4 * q + 2] = v.z;
+    c[4 * q + 3] = v.w;
+  }
+  unsigned S = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) S += c[j];
+  unsigned total;
+  const unsigned A = block_suffix_excl(S, &total, ctl);  // this block's elements above my bins
+  if (A < k && (threadIdx.x == 0 || A + S >= k)) {
+    // the floor is mine: the lowest of my bins with fewer than k above it
+    unsigned above = A;
+    int f = 0;
+#pragma unroll
+    for (int j = kPer - 1; j >= 0; --j) {
+      if (above < k) f = j;
+      above += c[j];
+    }
+    ctl->lo = (unsigned)(b0 + f);
+  }
+  if (A == 0u && S != 0u) {  // my bins hold the highest nonempty one
+    int tj = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (c[j] != 0u) tj = j;
+    ctl->top = (unsigned)(b0 + tj + 1);
+  }
+  if (total == 0u && threadIdx.x == 0) ctl->top = 0u;
+  __syncthreads();
+  const int l = (int)ctl->lo, top = (int)ctl->top;
+  *lo = l;
+  if (!split) {
+    *hi = top;
+    return true;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    c[j] = (b >= l && b < top) ? h[b] : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
+  // an atomic with return, so it has been performed by the arrival
+  if (threadIdx.x == 0 && top > 0) ctl->sink = atomicMax(&sync_pair[1], (unsigned)top);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int b = j * kThreads + threadIdx.x;
+    if (b >= l && b < top) offs[b] = c[j];
+  }
+  __syncthreads();  // also: every thread has read ctl->top before it is rewritten
+  if (!merge_wait_load(h, l, kMaxBins, g, sync_pair, true, target, skip_arrive, limit, ctl, status))
+    return false;
+  *hi = (int)ctl->top;
   return true;
 }
 
@@ -850,7 +935,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
   constexpr int U = SliceSrc<DT>::U;
-  unsigned top1 = 0u;  // 1 + highest first-digit bin this thread saw
   uint32_t gmax = 0u;                  // largest key of the group f0 saw last
   uint32_t mk[kChunks][kMarkSteps];    // largest key of each early step of this thread
 #pragma unroll
@@ -863,7 +947,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     for (int j = 0; j < U; ++j)
       if ((vm >> j) & 1u) {
         atomicAdd(&h[key[j] >> E::kShift0], 1u);
-        top1 = max(top1, (key[j] >> E::kShift0) + 1u);
         m = max(m, key[j]);
       }
     gmax = m;
@@ -906,11 +989,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   }
   __syncthreads();
   if (!ctl->ok) return false;
-  // Bins the first threshold can lie in: from this block's own lower bound
-  // up to its highest nonempty bin (and, after the merge, the row's).
-  int floor0;
-  unsigned top0;
-  local_bounds(h, k, top1, ctl, &floor0, &top0);
 
   // Counters of this call's parity; the other parity's are cleared below.
   const unsigned epoch = hdr.x, par = epoch & 1u;
@@ -945,20 +1023,19 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     }
     int lo = 0, hi = nb;
     if (t == 0) {
-      lo = floor0;
-      hi = (int)top0;
-    }
-    if (group > 1) {
-      const bool skip = p.test_skip_arrive && part == 0 && t == 0;
-      if (!group_merge(h, offs, lo, hi, nb, slot_hist + (size_t)t * kMaxBins, &slot->sync[par].arrive,
-                       top0, t == 0, (unsigned)group * (t + 1), skip, p.spin_limit_ns, ctl, status))
+      const bool skip = p.test_skip_arrive && part == 0;
+      if (!round0_bounds_merge(h, offs, k, group > 1, group > 1 ? slot_hist : nullptr,
+                               group > 1 ? &slot->sync[par].arrive : nullptr, (unsigned)group, skip,
+                               p.spin_limit_ns, ctl, status, &lo, &hi))
         return false;
-      hi = (int)ctl->top;
       // every block of the call has read the epoch: the next call may use the other set
-      if (t == 0 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
-    } else {
-      zero_counters(offs, nb);
+      if (group > 1 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
+    } else if (group > 1) {
+      if (!group_merge(h, offs, nb, slot_hist + (size_t)t * kMaxBins, &slot->sync[par].arrive,
+                       (unsigned)group * (t + 1), p.spin_limit_ns, ctl, status))
+        return false;
     }
+    if (group == 1) zero_counters(offs, nb);
     unsigned bin, above;
     if (!pick_bin_range(h, lo, hi, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
     const unsigned need = k_rem - above;
