@@ -79,6 +79,7 @@ struct Ctl {
   unsigned top;
   unsigned qn;                 // marked steps queued for a pass
   unsigned lo;                 // first-round floor bin of this block
+  unsigned emit_n;             // output slots taken by the final emission
   unsigned sink;               // keeps an atomic's returned value live
   unsigned red[4 * kWarps];
   unsigned queue[kQueueCap];   // first vector of each marked step
@@ -369,13 +370,10 @@ __device__ __forceinline__ void pick_and_suffix(unsigned* h, int nb, unsigned k_
 // (all threads call; every thread gets the totals).
 __device__ __forceinline__ void block_or_and(uint32_t& or_a, uint32_t& and_a, uint32_t& or_b,
                                              uint32_t& and_b, Ctl* ctl) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    or_a |= __shfl_xor_sync(0xffffffffu, or_a, off);
-    and_a &= __shfl_xor_sync(0xffffffffu, and_a, off);
-    or_b |= __shfl_xor_sync(0xffffffffu, or_b, off);
-    and_b &= __shfl_xor_sync(0xffffffffu, and_b, off);
-  }
+  or_a = __reduce_or_sync(0xffffffffu, or_a);
+  and_a = __reduce_and_sync(0xffffffffu, and_a);
+  or_b = __reduce_or_sync(0xffffffffu, or_b);
+  and_b = __reduce_and_sync(0xffffffffu, and_b);
   const unsigned warp = threadIdx.x >> 5;
   if (lane_id() == 0) {
     ctl->red[4 * warp + 0] = or_a;

@@ -563,11 +563,53 @@ __device__ __forceinline__ bool pick_bin_range(unsigned* h, int lo, int hi, int 
 // Finds the threshold bin of h[0..nb) and turns h into exclusive suffix sums;
 // false (and an error) if the counts are inconsistent, which cannot happen
 // unless memory was corrupted.
+// The bin of h[0, nb) holding the k_rem-th largest count from the top, with
+// the count above it and its own count (into ctl->pick_*), from one
+// block-wide scan over per-thread sums of kPer consecutive bins.  Leaves no
+// suffix sums behind.
+__device__ __forceinline__ void pick_scan(const unsigned* h, int nb, unsigned k_rem, Ctl* ctl) {
+  constexpr int kPer = kMaxBins / kThreads;
+  static_assert(kPer % 4 == 0, "bins per thread");
+  const int b0 = (int)threadIdx.x * kPer;
+  unsigned c[kPer];
+  if (b0 + kPer <= nb) {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(h + b0)[q];
+      c[4 * q] = v.x;
+      c[4 * q + 1] = v.y;
+      c[4 * q + 2] = v.z;
+      c[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) c[j] = b0 + j < nb ? h[b0 + j] : 0u;
+  }
+  unsigned S = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) S += c[j];
+  unsigned total;
+  const unsigned A = block_suffix_excl(S, &total, ctl);
+  if (A < k_rem && A + S >= k_rem) {
+    unsigned above = A;
+#pragma unroll
+    for (int j = kPer - 1; j >= 0; --j) {
+      if (above < k_rem && above + c[j] >= k_rem) {
+        ctl->pick_bin = (unsigned)(b0 + j);
+        ctl->pick_above = above;
+        ctl->pick_cnt = c[j];
+      }
+      above += c[j];
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ bool pick_bin(unsigned* h, int nb, unsigned k_rem, Ctl* ctl,
                                          unsigned* status, unsigned* bin, unsigned* above,
                                          unsigned* cnt) {
   if (threadIdx.x == 0) ctl->pick_bin = 0xFFFFFFFFu;
-  pick_and_suffix(h, nb, k_rem, ctl);
+  pick_scan(h, nb, k_rem, ctl);
   *bin = ctl->pick_bin;
   *above = ctl->pick_above;
   *cnt = ctl->pick_cnt;
@@ -818,6 +860,7 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   const unsigned out_base = k - k_rem;
   uint32_t vk = (or_k ^ and_k) & ~P.kmask;
   uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
+  if (threadIdx.x == 0) ctl->emit_n = 0u;  // read after the rounds' barriers
   unsigned sel = 0u;
   unsigned live = n;
   for (;;) {
@@ -851,17 +894,30 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
     }
     live = cnt;
   }
-  unsigned total;
-  unsigned slot = out_base + block_suffix_excl((unsigned)__popc(sel), &total, ctl);
+  // Distinct slots from out_base on: each warp takes a run of them with one
+  // shared add, its lanes place their candidates by ballot ranks.
+  const unsigned lane = lane_id(), lt = (1u << lane) - 1u;
+  unsigned m[kRegCand];
+  unsigned wtotal = 0u;
+#pragma unroll
+  for (int j = 0; j < kRegCand; ++j) {
+    m[j] = __ballot_sync(0xffffffffu, (sel >> j) & 1u);
+    wtotal += (unsigned)__popc(m[j]);
+  }
+  unsigned wbase = 0u;
+  if (lane == 0 && wtotal) wbase = atomicAdd(&ctl->emit_n, wtotal);
+  unsigned slot = out_base + __shfl_sync(0xffffffffu, wbase, 0);
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kRegCand; ++j) {
-    if (!((sel >> j) & 1u)) continue;
-    if (slot < k)
-      out_row[slot] = (int)(pmax - ci[j]);
-    else
-      bad = true;
-    ++slot;
+    if ((sel >> j) & 1u) {
+      const unsigned sj = slot + (unsigned)__popc(m[j] & lt);
+      if (sj < k)
+        out_row[sj] = (int)(pmax - ci[j]);
+      else
+        bad = true;
+    }
+    slot += (unsigned)__popc(m[j]);
   }
   if (bad) atomicOr(status, kStatInternal);
 }
