@@ -61,6 +61,8 @@ def _bind(path: str):
     i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
     lib.tks_oracle_topk_batch.argtypes = [vp, i32, i64, i64, vp, i64, vp]
     lib.tks_oracle_topk_batch.restype = ctypes.c_int
+    lib.tks_oracle_topk_batch_order.argtypes = [vp, i32, i64, i64, vp, i64, i32, vp]
+    lib.tks_oracle_topk_batch_order.restype = ctypes.c_int
     lib.tks_oracle_topk_f32.argtypes = [vp, i64, i64, vp]
     lib.tks_oracle_topk_f32.restype = ctypes.c_int
     lib.tks_oracle_selftest.argtypes = []
@@ -85,13 +87,14 @@ def load(path: str | None = None):
 
 
 def topk_indices(values: np.ndarray, k: int, row_len=None, dtype: str | None = None,
-                 lib=None) -> np.ndarray:
+                 lib=None, ordered: bool = False) -> np.ndarray:
     """Top-k index set of every row.
 
     ``values``: [batch, row_stride] (or 1-D for one row) float32, or uint16 holding
     bf16 bit patterns (``dtype="bf16"``).  ``row_len``: valid length per row
     (default: the whole stride).  Returns int32 [batch, k]: each row's selected
-    positions in ascending order, then -1 where the row has fewer than k values.
+    positions in ascending order (``ordered``: in rank order, largest value
+    first, ties by lower position), then -1 where the row has fewer than k values.
     """
     v = np.asarray(values)
     squeeze = v.ndim == 1
@@ -114,17 +117,17 @@ def topk_indices(values: np.ndarray, k: int, row_len=None, dtype: str | None = N
         rl = np.ascontiguousarray(np.broadcast_to(np.asarray(row_len, np.int32), (batch,)))
     out = np.empty((batch, int(k)), np.int32)
     lib = lib or load()
-    rc = lib.tks_oracle_topk_batch(v.ctypes.data, code, batch, stride, rl.ctypes.data,
-                                   int(k), out.ctypes.data)
+    rc = lib.tks_oracle_topk_batch_order(v.ctypes.data, code, batch, stride, rl.ctypes.data,
+                                         int(k), 1 if ordered else 0, out.ctypes.data)
     if rc != 0:
         raise OracleError({1: "invalid argument", 2: "NaN in a valid position",
                            3: "out of memory"}.get(rc, f"error {rc}"))
     return out[0] if squeeze else out
 
 
-def topk_workload(w, lib=None) -> np.ndarray:
+def topk_workload(w, lib=None, ordered: bool = False) -> np.ndarray:
     """Top-k of a ``workloads.Workload``."""
-    return topk_indices(w.values, w.k, w.row_len, w.dtype, lib=lib)
+    return topk_indices(w.values, w.k, w.row_len, w.dtype, lib=lib, ordered=ordered)
 
 
 __all__ = ["build", "load", "topk_indices", "topk_workload", "OracleError", "F32", "BF16"]

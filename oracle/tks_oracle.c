@@ -28,7 +28,10 @@
  *   - NaN in the valid prefix is outside the contract: the call fails;
  *   - if L < k the remaining k - L outputs are -1 (the flush of the
  *     selector's output buffer in section "5. Triton-TLE" pads with -1);
- *   - the returned set is sorted ascending, so that sets compare element-wise.
+ *   - the returned set is sorted ascending, so that sets compare element-wise;
+ *     the "ordered" entry points instead return the selected positions in
+ *     the order above (largest value first, ties by lower position), the
+ *     optional sorted output of the pseudocode's final step.
  *
  * Parity pins (brute force, rank counting, the page's base-10 digit
  * selection, closed forms, invariants) live in the test-suite.
@@ -118,8 +121,10 @@ static void sort_ascending_i64(int64_t *a, int64_t m)
     }
 }
 
-/* Top-k of one float row.  out has room for k entries. */
-int tks_oracle_topk_f32(const float *v, int64_t row_len, int64_t k, int32_t *out)
+/* Top-k of one float row.  out has room for k entries.  ordered = 0: the
+ * set in ascending position order; ordered = 1: in rank order. */
+int tks_oracle_topk_f32_order(const float *v, int64_t row_len, int64_t k, int32_t ordered,
+                              int32_t *out)
 {
     int64_t *pos, *tmp, i, take;
     if (row_len < 0 || k < 1 || (row_len > 0 && v == NULL) || out == NULL) return TKS_ORACLE_EINVAL;
@@ -139,7 +144,22 @@ int tks_oracle_topk_f32(const float *v, int64_t row_len, int64_t k, int32_t *out
     }
     for (i = 0; i < row_len; ++i) pos[i] = i;
     merge_sort_positions(v, pos, tmp, row_len);
-    sort_ascending_i64(pos, take);
+#if TKS_ORACLE_MUTANT == 7 /* rank order with ties reversed */
+    if (ordered) {
+        int64_t a = 0, b2;
+        while (a < take) {
+            b2 = a + 1;
+            while (b2 < take && v[pos[b2]] == v[pos[a]] && signbit(v[pos[b2]]) == signbit(v[pos[a]])) ++b2;
+            for (i = 0; i < (b2 - a) / 2; ++i) {
+                int64_t t = pos[a + i];
+                pos[a + i] = pos[b2 - 1 - i];
+                pos[b2 - 1 - i] = t;
+            }
+            a = b2;
+        }
+    }
+#endif
+    if (!ordered) sort_ascending_i64(pos, take);
     for (i = 0; i < take; ++i) out[i] = (int32_t)pos[i];
     for (i = take; i < k; ++i) out[i] = -1;
     free(pos);
@@ -159,7 +179,13 @@ static float widen_bf16(uint16_t b)
     return f;
 }
 
-int tks_oracle_topk_bf16(const uint16_t *b, int64_t row_len, int64_t k, int32_t *out)
+int tks_oracle_topk_f32(const float *v, int64_t row_len, int64_t k, int32_t *out)
+{
+    return tks_oracle_topk_f32_order(v, row_len, k, 0, out);
+}
+
+int tks_oracle_topk_bf16_order(const uint16_t *b, int64_t row_len, int64_t k, int32_t ordered,
+                               int32_t *out)
 {
     float *v;
     int64_t i;
@@ -168,16 +194,21 @@ int tks_oracle_topk_bf16(const uint16_t *b, int64_t row_len, int64_t k, int32_t 
     v = (float *)malloc((size_t)(row_len > 0 ? row_len : 1) * sizeof(float));
     if (v == NULL) return TKS_ORACLE_ENOMEM;
     for (i = 0; i < row_len; ++i) v[i] = widen_bf16(b[i]);
-    rc = tks_oracle_topk_f32(v, row_len, k, out);
+    rc = tks_oracle_topk_f32_order(v, row_len, k, ordered, out);
     free(v);
     return rc;
+}
+
+int tks_oracle_topk_bf16(const uint16_t *b, int64_t row_len, int64_t k, int32_t *out)
+{
+    return tks_oracle_topk_bf16_order(b, row_len, k, 0, out);
 }
 
 /* A batch laid out as rows of row_stride elements; dtype 0 = float32, 1 = bf16.
  * row_len may be NULL (every row has row_stride valid elements).
  * out is [batch][k]. */
-int tks_oracle_topk_batch(const void *values, int32_t dtype, int64_t batch, int64_t row_stride,
-                          const int32_t *row_len, int64_t k, int32_t *out)
+int tks_oracle_topk_batch_order(const void *values, int32_t dtype, int64_t batch, int64_t row_stride,
+                                const int32_t *row_len, int64_t k, int32_t ordered, int32_t *out)
 {
     int64_t r;
     if (batch < 0 || row_stride < 0 || k < 1 || (dtype != 0 && dtype != 1)) return TKS_ORACLE_EINVAL;
@@ -186,12 +217,20 @@ int tks_oracle_topk_batch(const void *values, int32_t dtype, int64_t batch, int6
         int rc;
         if (L < 0 || L > row_stride) return TKS_ORACLE_EINVAL;
         if (dtype == 0)
-            rc = tks_oracle_topk_f32((const float *)values + r * row_stride, L, k, out + r * k);
+            rc = tks_oracle_topk_f32_order((const float *)values + r * row_stride, L, k, ordered,
+                                           out + r * k);
         else
-            rc = tks_oracle_topk_bf16((const uint16_t *)values + r * row_stride, L, k, out + r * k);
+            rc = tks_oracle_topk_bf16_order((const uint16_t *)values + r * row_stride, L, k, ordered,
+                                            out + r * k);
         if (rc != TKS_ORACLE_OK) return rc;
     }
     return TKS_ORACLE_OK;
+}
+
+int tks_oracle_topk_batch(const void *values, int32_t dtype, int64_t batch, int64_t row_stride,
+                          const int32_t *row_len, int64_t k, int32_t *out)
+{
+    return tks_oracle_topk_batch_order(values, dtype, batch, row_stride, row_len, k, 0, out);
 }
 
 /* 0 when the build keeps subnormals distinct from zero and keeps -0.0 signed. */

@@ -25,6 +25,7 @@ What pins what:
 
 from __future__ import annotations
 
+import functools
 import itertools
 import math
 import os
@@ -192,6 +193,56 @@ def pin_rank_count(topk, seed=5):
             want = rank_count_topk(v, k)
             got = topk(v, k, None, W.F32)[0]
             assert np.array_equal(got, want), (v.size, k)
+
+
+def rank_order_topk(v, k):
+    """Rank-ordered top-k in closed form: the position whose count of positions
+    ranking before it is r goes to output slot r (r < k)  (O(L^2))."""
+    v = np.asarray(v, np.float32)
+    L = v.size
+    neg = np.signbit(v)
+    idx = np.arange(L)
+    vj, vi = v[:, None], v[None, :]
+    eq = vj == vi
+    before = (vj > vi) | (eq & (~neg[:, None] & neg[None, :])) | \
+             (eq & (neg[:, None] == neg[None, :]) & (idx[:, None] < idx[None, :]))
+    rank = before.sum(axis=0)
+    out = np.full(k, -1, np.int64)
+    sel = rank < k
+    out[rank[sel]] = idx[sel]
+    return out
+
+
+def brute_force_ordered(v, k):
+    """Rank order by pairwise comparison with the order's definition."""
+    order = sorted(range(len(v)), key=functools.cmp_to_key(
+        lambda i, j: -1 if _ranks_before(float(v[i]), i, float(v[j]), j) else 1))
+    take = min(k, len(v))
+    return order[:take] + [-1] * (k - take)
+
+
+def pin_rank_order(topk_ordered, seed=15):
+    """The rank-ordered oracle output against the closed form and, on tiny rows,
+    against pairwise brute force."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = [
+        rng.standard_normal(2048).astype(np.float32),
+        rng.integers(0, 6, size=1500).astype(np.float32) - 3.0,
+        W.straddle_row(rng, 2000),
+        W.bf16_bits_to_f32(W.bf16_mixed_zeros_subnormals(rng, 1800, 0.2, 0.2, 0.2)),
+        np.where(rng.random(1024) < 0.5, -np.inf, rng.standard_normal(1024)).astype(np.float32),
+    ]
+    for v in rows:
+        for k in (1, 7, 100, v.size // 2, v.size, v.size + 5):
+            got = topk_ordered(v, k, None, W.F32)[0]
+            assert np.array_equal(got, rank_order_topk(v, k)), (v.size, k)
+    pool = W.tiny_special_values()
+    for _ in range(200):
+        L = int(rng.integers(1, 9))
+        v = pool[rng.integers(0, pool.size, size=L)]
+        k = int(rng.integers(1, L + 2))
+        got = topk_ordered(v, k, None, W.F32)[0]
+        assert list(got) == brute_force_ordered(v, k), (v.tolist(), k, list(got))
 
 
 # ----------------------------------------------------------------------------

@@ -16,9 +16,40 @@ def _topk_with(lib):
     return topk
 
 
+def _topk_ordered_with(lib):
+    def topk(values, k, row_len, dtype):
+        return oracle.topk_indices(np.atleast_2d(values), k, row_len, dtype, lib=lib, ordered=True)
+    return topk
+
+
 @pytest.fixture(scope="module")
 def topk(oracle_lib):
     return _topk_with(oracle_lib)
+
+
+@pytest.fixture(scope="module")
+def topk_ordered(oracle_lib):
+    return _topk_ordered_with(oracle_lib)
+
+
+def test_rank_order_closed_form_and_brute_force(topk_ordered):
+    pins.pin_rank_order(topk_ordered)
+
+
+@pytest.mark.parametrize("name", sorted(W.NAMED))
+def test_rank_order_is_the_set_in_order(topk, topk_ordered, name):
+    """Rank-ordered output: the same set as the plain output, each entry ranked
+    before the next, -1 padding last."""
+    w = W.named(name)
+    plain = topk(w.values, w.k, w.row_len, w.dtype)
+    ordered = topk_ordered(w.values, w.k, w.row_len, w.dtype)
+    vals = w.values if w.dtype == W.F32 else W.bf16_bits_to_f32(w.values)
+    for r in range(w.batch):
+        assert np.array_equal(np.sort(ordered[r]), np.sort(plain[r]))
+        sel = ordered[r][ordered[r] >= 0]
+        v = vals[r]
+        for a, b in zip(sel[:-1], sel[1:]):
+            assert pins._ranks_before(float(v[a]), int(a), float(v[b]), int(b))
 
 
 def test_build_keeps_subnormals_and_signed_zero(oracle_lib):
@@ -102,7 +133,8 @@ def test_nan_rejected(topk):
 
 
 MUTANTS = {1: "ascending order", 2: "-0.0 above +0.0", 3: "sign rule dropped",
-           4: "ties to the highest position", 5: "one element short", 6: "bf16 widened from the wrong half"}
+           4: "ties to the highest position", 5: "one element short", 6: "bf16 widened from the wrong half",
+           7: "rank order with ties reversed"}
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
@@ -117,6 +149,7 @@ def test_pins_catch_planted_mistakes(tmp_path, mutant):
         lambda: pins.pin_closed_forms(t),
         lambda: pins.pin_bitkey_radix(t, W.fuzz_cases()[-4]),  # bf16 odd-stride rows
         lambda: pins.pin_rank_count(t),
+        lambda: pins.pin_rank_order(_topk_ordered_with(lib)),
     ]
     failed = 0
     for c in checks:
