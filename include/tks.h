@@ -98,6 +98,27 @@ int tks_topk_indices(const void *logits, const int32_t *row_len, int32_t batch,
                      void *stream);
 
 /*
+ * tks_topk_indices_sorted - tks_topk_indices followed by the rank ordering of
+ * each row's result: slots 0 .. min(k, len)-1 of row r hold the selected
+ * positions ordered by value, largest first (+0.0 before -0.0), equal values
+ * by lower position first, i.e. the selector's own order; slots min(k, len)
+ * .. k-1 hold -1.  This is the optional sorted output of the radix_topk
+ * pseudocode's final step ("Technical Deep Dive | ... Triton-TLE ... TopK
+ * Selector", section "02. Traditional GPU Approach: Radix Selection").
+ *
+ * Arguments, ownership, workspace and device-side errors are those of
+ * tks_topk_indices, with 1 <= k <= TKS_SORTED_K_MAX (a larger k returns
+ * TKS_E_INVAL and launches nothing).  Two kernels are enqueued on `stream`:
+ * the selection, then one block per row that reads the row's k positions
+ * and their logits and sorts them on chip; the second waits for the first.
+ * Returns TKS_E_CUDA if the second launch fails (the first is enqueued).
+ */
+#define TKS_SORTED_K_MAX 16384
+int tks_topk_indices_sorted(const void *logits, const int32_t *row_len, int32_t batch,
+                            int64_t row_stride, int32_t k, int32_t dtype, int32_t *out_idx,
+                            void *stream);
+
+/*
  * tks_device_status - synchronise `stream`, then return and clear the first
  * device-side error recorded by calls on it (TKS_OK if none, or if no call
  * was ever made on it).  After an error the stream's workspace is re-zeroed,

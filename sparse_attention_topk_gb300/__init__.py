@@ -32,6 +32,7 @@ TKS_E_TOO_LARGE = 7
 TKS_NOALLOC_MAX_ROWS = 8
 
 TKS_K_MAX = 1 << 24
+TKS_SORTED_K_MAX = 16384
 
 TKS_OPT_FORCE_GROUP = 1
 TKS_OPT_SPIN_LIMIT_NS = 2
@@ -49,6 +50,7 @@ SIGNATURES = {
     "tks_set_option": (ctypes.c_int, [ctypes.c_int, _I64]),
     "tks_plan": (ctypes.c_int, [_I32, _I64, _I32, _I32, _VP, _VP]),
     "tks_topk_indices_noalloc": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
+    "tks_topk_indices_sorted": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
 }
 
 _lock = threading.Lock()
@@ -132,6 +134,16 @@ def topk_indices_raw(logits_ptr: int, row_len_ptr: int | None, batch: int, row_s
         ctypes.c_void_p(stream_handle or 0)))
 
 
+def topk_indices_sorted_raw(logits_ptr: int, row_len_ptr: int | None, batch: int,
+                            row_stride: int, k: int, dtype: int, out_ptr: int,
+                            stream_handle: int | None = None) -> int:
+    """Direct call of tks_topk_indices_sorted (rank-ordered output, k <= TKS_SORTED_K_MAX)."""
+    return int(load().tks_topk_indices_sorted(
+        ctypes.c_void_p(logits_ptr), ctypes.c_void_p(row_len_ptr or 0), int(batch),
+        int(row_stride), int(k), int(dtype), ctypes.c_void_p(out_ptr),
+        ctypes.c_void_p(stream_handle or 0)))
+
+
 def topk_indices_noalloc_raw(logits_ptr: int, row_len_ptr: int | None, batch: int,
                              row_stride: int, k: int, dtype: int, out_ptr: int,
                              stream_handle: int | None = None) -> int:
@@ -152,15 +164,17 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
-def topk_indices(logits, k: int, row_len=None, out=None, stream=None):
+def topk_indices(logits, k: int, row_len=None, out=None, stream=None, sorted: bool = False):
     """Top-k positions of every row of a CUDA tensor.
 
     ``logits``: float32 or bfloat16 CUDA tensor [batch, n] (or [n]) whose last
     dimension is contiguous; rows may be padded (row stride = ``logits.stride(0)``).
     ``row_len``: optional int32 CUDA tensor [batch] of valid lengths (<= n).
     ``out``: optional int32 CUDA tensor [batch, k] (contiguous) to fill.
-    Returns int32 [batch, k] (or [k]): each row holds its selected positions in
-    unspecified order, then -1 where the row has fewer than k elements.
+    ``sorted``: rank order (largest value first, ties by lower position;
+    tks_topk_indices_sorted, k <= TKS_SORTED_K_MAX) instead of unspecified order.
+    Returns int32 [batch, k] (or [k]): each row holds its selected positions,
+    then -1 where the row has fewer than k elements.
     """
     import torch
 
@@ -193,19 +207,19 @@ def topk_indices(logits, k: int, row_len=None, out=None, stream=None):
               and tuple(out.shape) == (batch, k)):
         raise ValueError("out must be a contiguous int32 CUDA tensor [batch, k]")
     with torch.cuda.device(x.device):
-        rc = topk_indices_raw(x.data_ptr() if x.numel() else 0, rl_ptr, batch,
-                              row_stride if n > 0 else 0, k, dt, out.data_ptr(),
-                              _stream_handle(stream))
+        call = topk_indices_sorted_raw if sorted else topk_indices_raw
+        rc = call(x.data_ptr() if x.numel() else 0, rl_ptr, batch,
+                  row_stride if n > 0 else 0, k, dt, out.data_ptr(), _stream_handle(stream))
     if rc != TKS_OK:
-        raise TksError(rc, "tks_topk_indices")
+        raise TksError(rc, "tks_topk_indices_sorted" if sorted else "tks_topk_indices")
     return out[0] if squeeze else out
 
 
 __all__ = [
-    "topk_indices", "topk_indices_raw", "topk_indices_noalloc_raw", "device_status", "set_option", "plan", "release",
+    "topk_indices", "topk_indices_raw", "topk_indices_noalloc_raw", "topk_indices_sorted_raw", "device_status", "set_option", "plan", "release",
     "status_string", "version", "load", "lib_path", "build", "TksError", "SIGNATURES",
     "TKS_F32", "TKS_BF16", "TKS_OK", "TKS_E_INVAL", "TKS_E_UNSUPPORTED", "TKS_E_CUDA",
     "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_E_TOO_LARGE", "TKS_NOALLOC_MAX_ROWS",
-    "TKS_K_MAX", "TKS_OPT_FORCE_GROUP",
+    "TKS_K_MAX", "TKS_SORTED_K_MAX", "TKS_OPT_FORCE_GROUP",
     "TKS_OPT_SPIN_LIMIT_NS", "TKS_OPT_MIN_PER_BLOCK", "TKS_OPT_TEST_SKIP_ARRIVE",
 ]

@@ -42,6 +42,7 @@
 
 #include "tks.h"
 #include "tks_device.cuh"
+#include "tks_internal.h"
 
 namespace tks {
 
@@ -1497,6 +1498,20 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
   cudaError_t e = dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0>, p)
                                    : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TKS_E_CUDA;
+  }
+  return TKS_OK;
+}
+
+extern "C" int tks_topk_indices_sorted(const void* logits, const int32_t* row_len, int32_t batch,
+                                       int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
+                                       void* stream) {
+  if (k > kOrderKMax) return TKS_E_INVAL;
+  const int rc = tks_topk_indices(logits, row_len, batch, row_stride, k, dtype, out_idx, stream);
+  if (rc != TKS_OK || batch == 0) return rc;
+  if (launch_rank_order(logits, batch, row_stride, k, dtype, out_idx, (cudaStream_t)stream) !=
+      cudaSuccess) {
     cudaGetLastError();
     return TKS_E_CUDA;
   }

@@ -58,6 +58,13 @@ def test_invalid_arguments_rejected_before_any_cuda_call(args):
     assert tks.topk_indices_raw(logits, row_len, batch, stride, k, dtype, out, 0) == tks.TKS_E_INVAL
 
 
+def test_sorted_entry_validates_like_the_plain_one():
+    assert tks.topk_indices_sorted_raw(16, None, 1, 8, tks.TKS_SORTED_K_MAX + 1, 0, 16, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_sorted_raw(16, None, 1, 8, 0, 0, 16, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_sorted_raw(16, None, 1, 8, 1, 7, 16, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_sorted_raw(0, None, 0, 8, 1, 0, 16, 0) == tks.TKS_OK
+
+
 def test_empty_batch_is_a_no_op():
     assert tks.topk_indices_raw(0, None, 0, 8, 1, 0, 16, 0) == tks.TKS_OK
 
