@@ -456,7 +456,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_1m_masked", choices=sorted(W.NAMED))
+    ap.add_argument("--workload", default="decode_1m_masked", choices=sorted(W.NAMED) + sorted(W.EXTRA))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args(argv)

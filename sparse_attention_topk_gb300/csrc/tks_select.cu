@@ -44,6 +44,10 @@
 #include "tks_device.cuh"
 #include "tks_internal.h"
 
+#ifndef EMIT_FIRST_DIRECT
+#define EMIT_FIRST_DIRECT 1
+#endif
+
 namespace tks {
 
 struct Params {
@@ -686,6 +690,66 @@ __device__ __forceinline__ void emit_round(const Src& src, const Prefix& P, Digi
   if (bad) atomicOr(status, kStatInternal);
 }
 
+// First-round emission from a resident slice, as a plain pass: whole vectors
+// (four loads in flight per thread), one compare per element (in the first
+// round an element is written exactly when its key reaches t0), and the
+// write path only for the elements that pass.  The partial edge vectors go
+// through visit_edges.
+template <int DT>
+__device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uint32_t t0,
+                                                    const Digit& D, unsigned bin, int end,
+                                                    unsigned base, const unsigned* suf,
+                                                    unsigned* offs, int32_t* out_row, unsigned k,
+                                                    uint2* cand, bool cand_global, unsigned cap,
+                                                    unsigned* status) {
+  using E = Elt<DT>;
+  constexpr int U = E::V;
+  constexpr int B = kPassVecs;
+  bool bad = false;
+  auto write = [&](uint32_t key, int pos) {
+    const uint32_t d = key >> D.shift;
+    const unsigned o = atomicAdd(&offs[d], 1u);  // rank inside the bin, row-wide
+    if (end == kEndCollect && d == bin) {
+      if (o < cap)
+        put_cand(cand, o, key, pos, cand_global);
+      else
+        bad = true;
+    } else {
+      const unsigned slot = base + suf[d] + o;
+      if (slot < k)
+        out_row[slot] = pos;
+      else
+        bad = true;
+    }
+  };
+  const Slice& s = src.s;
+  const uint4* sv = reinterpret_cast<const uint4*>(src.sm);
+  const int va = s.vb0, vb = s.vb0 + s.nbv;
+  for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads) {
+    uint4 x[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kThreads;
+      x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kThreads;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t key = E::key(E::lane(x[b], j));
+        if (v < vb && key >= t0) write(key, s.o + v * U + j);
+      }
+    }
+  }
+  src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if (((vm >> j) & 1u) && key[j] >= t0) write(key[j], pos[j]);
+  });
+  if (bad) atomicOr(status, kStatInternal);
+}
+
 // The highest still-varying bits (at most `width`) of the composite key:
 // value key first, then the inverted position.  False when nothing varies.
 __device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, int width, Digit* D) {
@@ -1100,8 +1164,13 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     // (a round that only passes the threshold on, with nothing above its bin
     // anywhere in the row, has nothing to emit)
     if (end != kEndAbove || above != 0u) {
-      emit_round(SliceMarkSrc<DT>{src, mk, P.kpref | (D.on_pos ? 0u : bin << D.shift), ctl}, P, D,
-                 bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
+      const uint32_t t0 = (end == kEndAbove ? bin + 1u : bin) << D.shift;
+      if (t == 0 && s.resident && !(end == kEndAbove && t0 == 0u) && EMIT_FIRST_DIRECT)
+        emit_first_resident(src, t0, D, bin, end, base, h, offs, out_row, k, cand, group > 1, cap,
+                            status);
+      else
+        emit_round(SliceMarkSrc<DT>{src, mk, P.kpref | (D.on_pos ? 0u : bin << D.shift), ctl}, P,
+                   D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
     }
     prefix_extend(P, D, bin);
     base += above;

@@ -179,8 +179,25 @@ NAMED = {
 }
 
 
+def prefill_causal(seed: int = 6) -> Workload:
+    """A prefill-like batch: 512 query rows over a 32K context with causal
+    lengths (row r sees 64 (r + 1) tokens), N(0,1) fp32 logits, k=2048.  Not
+    one of the five named configurations: the large-batch case that the
+    page's batch=64 results point to, at the scale of a prefill chunk."""
+    rng = _rng(seed)
+    batch, stride = 512, 32768
+    lens = (64 * (np.arange(batch) + 1)).astype(np.int32)
+    v = rng.standard_normal((batch, stride)).astype(np.float32)
+    _poison_tails(v, lens, F32)
+    return Workload("prefill_causal", v, lens, 2048, F32,
+                    "batch=512, row_stride=32768 fp32, causal lengths 64(r+1), N(0,1), k=2048")
+
+
+EXTRA = {"prefill_causal": prefill_causal}
+
+
 def named(name: str) -> Workload:
-    return NAMED[name]()
+    return NAMED[name]() if name in NAMED else EXTRA[name]()
 
 
 # ----------------------------------------------------------------------------
@@ -287,7 +304,7 @@ def expected_top_plateau(n: int) -> tuple[int, int]:
 
 
 __all__ = [
-    "Workload", "F32", "BF16", "NAMED", "named", "fuzz_cases", "random_rows", "from_rows",
+    "Workload", "F32", "BF16", "NAMED", "EXTRA", "named", "fuzz_cases", "random_rows", "from_rows",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "as_float32", "bf16_ramp", "tiny_special_values",
     "expected_top_plateau", "decode_4k", "decode_128k", "decode_1m_masked", "batch64_ragged",
     "batch4_1m_bf16", "gumbel_open", "bf16_mixed_zeros_subnormals", "straddle_row",
