@@ -750,6 +750,81 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
   if (bad) atomicOr(status, kStatInternal);
 }
 
+// A later round over a resident slice as a plain pass (as emit_first_resident):
+// elements that match the prefix P go into the digit-D histogram h (count)
+// or, when emitting, are written if their digit is above bin (or equal, per
+// end).  Vectors whose largest key cannot match P are skipped.
+template <int DT, bool kEmit>
+__device__ __forceinline__ void later_pass_resident(const SliceSrc<DT>& src, const Prefix& P,
+                                                    const Digit& D, uint32_t pmax, unsigned* h,
+                                                    unsigned bin, int end, unsigned base,
+                                                    const unsigned* suf, unsigned* offs,
+                                                    int32_t* out_row, unsigned k, uint2* cand,
+                                                    bool cand_global, unsigned cap,
+                                                    unsigned* status) {
+  using E = Elt<DT>;
+  constexpr int U = E::V;
+  constexpr int B = kPassVecs;
+  bool bad = false;
+  auto element = [&](uint32_t key, int pos) {
+    const uint32_t inv = pmax - (uint32_t)pos;
+    if ((key & P.kmask) != P.kpref || (inv & P.pmask) != P.ppref) return;
+    const uint32_t d = digit_value(D, key, inv);
+    if (!kEmit) {
+      atomicAdd(&h[d], 1u);
+      return;
+    }
+    if (d < bin || (d == bin && end == kEndAbove)) return;
+    const unsigned o = atomicAdd(&offs[d], 1u);  // rank inside the bin, row-wide
+    if (end == kEndCollect && d == bin) {
+      if (o < cap)
+        put_cand(cand, o, key, pos, cand_global);
+      else
+        bad = true;
+    } else {
+      const unsigned slot = base + suf[d] + o;
+      if (slot < k)
+        out_row[slot] = pos;
+      else
+        bad = true;
+    }
+  };
+  // keys at or above this can match the prefix (it is a leading-bits prefix)
+  const uint32_t kmin = P.kpref;
+  const Slice& s = src.s;
+  const uint4* sv = reinterpret_cast<const uint4*>(src.sm);
+  const int va = s.vb0, vb = s.vb0 + s.nbv;
+  for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads) {
+    uint4 x[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kThreads;
+      x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int v = v0 + b * kThreads;
+      if (v >= vb) continue;
+      uint32_t key[U];
+      uint32_t m = 0u;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        key[j] = E::key(E::lane(x[b], j));
+        m = max(m, key[j]);
+      }
+      if (m < kmin) continue;
+#pragma unroll
+      for (int j = 0; j < U; ++j) element(key[j], s.o + v * U + j);
+    }
+  }
+  src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if ((vm >> j) & 1u) element(key[j], pos[j]);
+  });
+  if (bad) atomicOr(status, kStatInternal);
+}
+
 // The highest still-varying bits (at most `width`) of the composite key:
 // value key first, then the inverted position.  False when nothing varies.
 __device__ __forceinline__ bool next_digit(uint32_t& vk, uint32_t& vp, int width, Digit* D) {
@@ -1139,7 +1214,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (t > 0) {
       zero_counters(h, nb);
       __syncthreads();
-      hist_round(SliceMarkSrc<DT>{src, mk, P.kpref, ctl}, h, P, D, pmax);
+      if (s.resident && EMIT_FIRST_DIRECT)
+        later_pass_resident<DT, false>(src, P, D, pmax, h, 0u, 0, 0u, nullptr, nullptr, nullptr, 0u,
+                                       nullptr, false, 0u, status);
+      else
+        hist_round(SliceMarkSrc<DT>{src, mk, P.kpref, ctl}, h, P, D, pmax);
       __syncthreads();
     }
     int lo = 0, hi = nb;
@@ -1168,6 +1247,9 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       if (t == 0 && s.resident && !(end == kEndAbove && t0 == 0u) && EMIT_FIRST_DIRECT)
         emit_first_resident(src, t0, D, bin, end, base, h, offs, out_row, k, cand, group > 1, cap,
                             status);
+      else if (t > 0 && s.resident && EMIT_FIRST_DIRECT)
+        later_pass_resident<DT, true>(src, P, D, pmax, nullptr, bin, end, base, h, offs, out_row, k,
+                                      cand, group > 1, cap, status);
       else
         emit_round(SliceMarkSrc<DT>{src, mk, P.kpref | (D.on_pos ? 0u : bin << D.shift), ctl}, P,
                    D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
