@@ -26,8 +26,6 @@ constexpr int kLocalCandCap = 4096;          // (key, position) pairs kept by a 
 constexpr int kGroupCandCap = kSliceBytes / 8;  // pairs the finishing block can hold
 constexpr int kChunks = 2;                   // bulk copies (and mbarriers) per slice
 constexpr int kPassVecs = 4;                 // vectors a thread loads per step of a pass
-constexpr int kMarkSteps = 4;                // first-pass steps per chunk whose key maxima are kept
-constexpr int kQueueCap = 160;               // marked steps a later pass visits
 
 // Dynamic shared memory layout.
 constexpr int kHistOff = 0;                          // counts, then exclusive suffix sums
@@ -77,12 +75,10 @@ struct Ctl {
   unsigned pick_bin, pick_above, pick_cnt;
   unsigned ok;
   unsigned top;
-  unsigned qn;                 // marked steps queued for a pass
   unsigned lo;                 // first-round floor bin of this block
   unsigned emit_n;             // output slots taken by the final emission
   unsigned sink;               // keeps an atomic's returned value live
   unsigned red[4 * kWarps];
-  unsigned queue[kQueueCap];   // first vector of each marked step
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block fits");
 

@@ -44,10 +44,6 @@
 #include "tks_device.cuh"
 #include "tks_internal.h"
 
-#ifndef EMIT_FIRST_DIRECT
-#define EMIT_FIRST_DIRECT 1
-#endif
-
 namespace tks {
 
 struct Params {
@@ -159,37 +155,6 @@ struct SliceSrc {
     }
   }
 
-  // As visit_range, and keeps the largest key of each of this thread's
-  // first kMarkSteps steps (kPassVecs vectors each) in mk[step]; later steps
-  // keep nothing.  f must also leave the largest key of its group in *gmax.
-  template <class F>
-  __device__ __forceinline__ void visit_range_mark(int va, int vb, uint32_t (&mk)[kMarkSteps],
-                                                   const uint32_t* gmax, F&& f) const {
-    constexpr int B = kPassVecs;
-    const uint4* sv = reinterpret_cast<const uint4*>(sm);
-    int step = 0;
-    for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads, ++step) {
-      uint4 x[B];
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const int v = v0 + b * kThreads;
-        x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
-      }
-      uint32_t m = 0u;
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const int v = v0 + b * kThreads;
-        if (v < vb) {
-          vec(x[b], s.o + v * U, (1u << U) - 1u, f);
-          m = max(m, *gmax);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kMarkSteps; ++q)
-        if (step == q) mk[q] = m;
-    }
-  }
-
   // The partial first and last vectors of the on-chip copy (threads 0 and 1).
   template <class F>
   __device__ __forceinline__ void visit_edges(F&& f) const {
@@ -245,70 +210,6 @@ struct SliceSrc {
       visit_edges(f);
     } else {
       visit_global(f);
-    }
-  }
-};
-
-// A slice seen through the step maxima of the first pass: a pass
-// with threshold `thr` visits every element whose key is at least thr, and
-// few others.  Each thread queues its steps whose largest key reaches thr
-// (steps without a kept maximum always), then the block visits the queued
-// steps' vectors together, one vector per thread, so the rare elements above
-// a high threshold cost one short step instead of a pass over the slice.
-// Falls back to the whole slice when the queue overflows, and for slices
-// streamed from global memory.  Every thread of the block must call visit().
-template <int DT>
-struct SliceMarkSrc {
-  static constexpr int U = Elt<DT>::V;
-  const SliceSrc<DT>& src;
-  const uint32_t (&mk)[kChunks][kMarkSteps];
-  uint32_t thr;
-  Ctl* ctl;
-  // Whether step `step` of chunk c of this thread may hold a key >= thr.
-  __device__ __forceinline__ bool marked(int c, int step) const {
-    uint32_t m = 0xFFFFFFFFu;  // steps past the kept ones: unknown
-#pragma unroll
-    for (int q = 0; q < kMarkSteps; ++q)
-      if (step == q) m = c == 0 ? mk[0][q] : mk[1][q];
-    return m >= thr;
-  }
-  template <class F>
-  __device__ __forceinline__ void visit(F&& f) const {
-    constexpr int B = kPassVecs;
-    const Slice& s = src.s;
-    if (!s.resident) {  // streamed slices keep no maxima
-      src.visit_global(f);
-      return;
-    }
-    const int mid = s.vb0 + s.nbv / kChunks;  // end of chunk 0 (kChunks == 2)
-    static_assert(kChunks == 2, "chunk layout");
-    // queue this thread's marked steps (a few shared atomics per block in the
-    // usual case; measured faster than placing them by a block-wide scan)
-    if (threadIdx.x == 0) ctl->qn = 0u;
-    __syncthreads();
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const int va = c == 0 ? s.vb0 : mid, vb = c == 0 ? mid : s.vb0 + s.nbv;
-      int step = 0;
-      for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads, ++step)
-        if (marked(c, step)) {
-          const unsigned i = atomicAdd(&ctl->qn, 1u);
-          if (i < (unsigned)kQueueCap) ctl->queue[i] = (unsigned)v0;
-        }
-    }
-    __syncthreads();
-    const unsigned n = ctl->qn;
-    src.visit_edges(f);
-    if (n > (unsigned)kQueueCap) {
-      src.visit_range(s.vb0, s.vb0 + s.nbv, f);
-      return;
-    }
-    const uint4* sv = reinterpret_cast<const uint4*>(src.sm);
-    for (unsigned e = threadIdx.x; e < n * B; e += kThreads) {
-      const int v0 = (int)ctl->queue[e / B];
-      const int v = v0 + (int)(e % B) * kThreads;
-      const int vb = v0 < mid ? mid : s.vb0 + s.nbv;
-      if (v < vb) src.vec(sv[v], s.o + v * U, (1u << U) - 1u, f);
     }
   }
 };
@@ -1131,21 +1032,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
   constexpr int U = SliceSrc<DT>::U;
-  uint32_t gmax = 0u;                  // largest key of the group f0 saw last
-  uint32_t mk[kChunks][kMarkSteps];    // largest key of each early step of this thread
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-    for (int q = 0; q < kMarkSteps; ++q) mk[c][q] = 0u;
   auto f0 = [&](const uint32_t(&key)[U], const int(&)[U], unsigned vm) {
-    uint32_t m = 0u;
 #pragma unroll
     for (int j = 0; j < U; ++j)
-      if ((vm >> j) & 1u) {
-        atomicAdd(&h[key[j] >> E::kShift0], 1u);
-        m = max(m, key[j]);
-      }
-    gmax = m;
+      if ((vm >> j) & 1u) atomicAdd(&h[key[j] >> E::kShift0], 1u);
   };
   if (s.resident) {
     const int vb0 = s.vb0, nbv = s.nbv;
@@ -1176,7 +1066,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       if (c1 > c0) {
         mbar_wait_bounded(&ctl->mbar[c], (phase_bits >> c) & 1u, p.spin_limit_ns, ctl, status);
         phase_bits ^= 1u << c;
-        src.visit_range_mark(vb0 + c0, vb0 + c1, mk[c], &gmax, f0);
+        src.visit_range(vb0 + c0, vb0 + c1, f0);
       }
     }
   } else {
@@ -1214,11 +1104,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (t > 0) {
       zero_counters(h, nb);
       __syncthreads();
-      if (s.resident && EMIT_FIRST_DIRECT)
+      if (s.resident)
         later_pass_resident<DT, false>(src, P, D, pmax, h, 0u, 0, 0u, nullptr, nullptr, nullptr, 0u,
                                        nullptr, false, 0u, status);
       else
-        hist_round(SliceMarkSrc<DT>{src, mk, P.kpref, ctl}, h, P, D, pmax);
+        hist_round(src, h, P, D, pmax);
       __syncthreads();
     }
     int lo = 0, hi = nb;
@@ -1244,15 +1134,15 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     // anywhere in the row, has nothing to emit)
     if (end != kEndAbove || above != 0u) {
       const uint32_t t0 = (end == kEndAbove ? bin + 1u : bin) << D.shift;
-      if (t == 0 && s.resident && !(end == kEndAbove && t0 == 0u) && EMIT_FIRST_DIRECT)
+      if (t == 0 && s.resident && !(end == kEndAbove && t0 == 0u))
         emit_first_resident(src, t0, D, bin, end, base, h, offs, out_row, k, cand, group > 1, cap,
                             status);
-      else if (t > 0 && s.resident && EMIT_FIRST_DIRECT)
+      else if (s.resident)
         later_pass_resident<DT, true>(src, P, D, pmax, nullptr, bin, end, base, h, offs, out_row, k,
                                       cand, group > 1, cap, status);
       else
-        emit_round(SliceMarkSrc<DT>{src, mk, P.kpref | (D.on_pos ? 0u : bin << D.shift), ctl}, P,
-                   D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap, status);
+        emit_round(src, P, D, bin, end, base, h, offs, pmax, out_row, k, cand, group > 1, cap,
+                   status);
     }
     prefix_extend(P, D, bin);
     base += above;
