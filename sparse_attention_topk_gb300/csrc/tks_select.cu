@@ -121,6 +121,12 @@ struct SliceSrc {
   const unsigned char* sm;   // on-chip copy (resident slices)
   Slice s;
 
+  // The key of position pos of this slice (on chip when resident).
+  __device__ __forceinline__ uint32_t key_at(int pos) const {
+    using E = Elt<DT>;
+    return E::key(s.resident ? E::load(sm, pos - s.o) : E::load(row, pos));
+  }
+
   template <class F>
   __device__ __forceinline__ void vec(const uint4& x, int i0, unsigned vm, F& f) const {
     using E = Elt<DT>;
@@ -633,14 +639,22 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
       const int v = v0 + b * kThreads;
       x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
     }
+    // which of the B * U elements are written (a compact unrolled test) ...
+    unsigned sel = 0u;
 #pragma unroll
     for (int b = 0; b < B; ++b) {
       const int v = v0 + b * kThreads;
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t key = E::key(E::lane(x[b], j));
-        if (v < vb && key >= t0) write(key, s.o + v * U + j);
-      }
+      for (int j = 0; j < U; ++j)
+        sel |= (v < vb && E::key(E::lane(x[b], j)) >= t0 ? 1u : 0u) << (b * U + j);
+    }
+    // ... then one copy of the write path for those (rare) elements, keys
+    // re-read from shared memory, so the loop stays small
+    while (sel) {
+      const int q = __ffs((int)sel) - 1;
+      sel &= sel - 1u;
+      const int pos = s.o + (v0 + (q / U) * kThreads) * U + q % U;
+      write(src.key_at(pos), pos);
     }
   }
   src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
@@ -702,20 +716,45 @@ __device__ __forceinline__ void later_pass_resident(const SliceSrc<DT>& src, con
       const int v = v0 + b * kThreads;
       x[b] = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
     }
+    if (!kEmit) {
+      // counting: a few operations per element, all inline
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int v = v0 + b * kThreads;
-      if (v >= vb) continue;
-      uint32_t key[U];
-      uint32_t m = 0u;
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
+        if (v >= vb) continue;
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        key[j] = E::key(E::lane(x[b], j));
-        m = max(m, key[j]);
+        for (int j = 0; j < U; ++j) {
+          const uint32_t key = E::key(E::lane(x[b], j));
+          if (key < kmin) continue;
+          const int pos = s.o + v * U + j;
+          const uint32_t inv = pmax - (uint32_t)pos;
+          if ((key & P.kmask) == P.kpref && (inv & P.pmask) == P.ppref)
+            atomicAdd(&h[digit_value(D, key, inv)], 1u);
+        }
       }
-      if (m < kmin) continue;
+    } else {
+      // emitting: which elements are written (a compact unrolled test), then
+      // one copy of the write path for those, so the loop stays small
+      unsigned sel = 0u;
 #pragma unroll
-      for (int j = 0; j < U; ++j) element(key[j], s.o + v * U + j);
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const uint32_t key = E::key(E::lane(x[b], j));
+          const uint32_t inv = pmax - (uint32_t)(s.o + v * U + j);
+          const uint32_t d = digit_value(D, key, inv);
+          const bool w = v < vb && (key & P.kmask) == P.kpref && (inv & P.pmask) == P.ppref &&
+                         (d > bin || (d == bin && end != kEndAbove));
+          sel |= (w ? 1u : 0u) << (b * U + j);
+        }
+      }
+      while (sel) {
+        const int q = __ffs((int)sel) - 1;
+        sel &= sel - 1u;
+        const int pos = s.o + (v0 + (q / U) * kThreads) * U + q % U;
+        element(src.key_at(pos), pos);
+      }
     }
   }
   src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
