@@ -24,7 +24,10 @@ constexpr int kMaxRounds = 6;                // fp32: 3 key digits + up to 3 pos
 constexpr int kSliceBytes = 160 * 1024;      // on-chip copy of a block's slice of the row
 constexpr int kLocalCandCap = 4096;          // (key, position) pairs kept by a lone block
 constexpr int kGroupCandCap = kSliceBytes / 8;  // pairs the finishing block can hold
-constexpr int kChunks = 2;                   // bulk copies (and mbarriers) per slice
+#ifndef TKS_CHUNKS
+#define TKS_CHUNKS 1
+#endif
+constexpr int kChunks = TKS_CHUNKS;          // bulk copies (and mbarriers) per slice
 constexpr int kPassVecs = 4;                 // vectors a thread loads per step of a pass
 
 // Dynamic shared memory layout.
