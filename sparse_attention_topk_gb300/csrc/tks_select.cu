@@ -654,7 +654,7 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
       const int q = __ffs((int)sel) - 1;
       sel &= sel - 1u;
       const int pos = s.o + (v0 + (q / U) * kThreads) * U + q % U;
-      write(src.key_at(pos), pos);
+      write(E::key(E::load(src.sm, pos - s.o)), pos);  // resident: on chip
     }
   }
   src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
@@ -753,7 +753,7 @@ __device__ __forceinline__ void later_pass_resident(const SliceSrc<DT>& src, con
         const int q = __ffs((int)sel) - 1;
         sel &= sel - 1u;
         const int pos = s.o + (v0 + (q / U) * kThreads) * U + q % U;
-        element(src.key_at(pos), pos);
+        element(E::key(E::load(src.sm, pos - s.o)), pos);  // resident: on chip
       }
     }
   }
