@@ -149,13 +149,18 @@ int tks_release(void);
  *   TKS_OPT_TEST_SKIP_ARRIVE test only: 1 makes the first block of each row
  *                            skip its first arrival, so the others' waits run
  *                            out and report TKS_E_TIMEOUT; 0 = off
- * Returns TKS_E_INVAL for an unknown option or a negative value.
+ *   TKS_OPT_FORCE_THREADS    threads per block: 0 = automatic (512 for rows
+ *                            split into slices of 48 KiB or more, else 256),
+ *                            or 256 or 512
+ * Returns TKS_E_INVAL for an unknown option, a negative value or (for
+ * TKS_OPT_FORCE_THREADS) a block size other than 0, 256 or 512.
  */
 typedef enum {
     TKS_OPT_FORCE_GROUP = 1,
     TKS_OPT_SPIN_LIMIT_NS = 2,
     TKS_OPT_MIN_PER_BLOCK = 3,
-    TKS_OPT_TEST_SKIP_ARRIVE = 4
+    TKS_OPT_TEST_SKIP_ARRIVE = 4,
+    TKS_OPT_FORCE_THREADS = 5
 } tks_option;
 int tks_set_option(int option, int64_t value);
 

@@ -13,9 +13,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libtks.so")
 
-SOURCES = [os.path.join(CSRC, "tks_select.cu"), os.path.join(CSRC, "tks_order.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "tks_device.cuh"), os.path.join(CSRC, "tks_internal.h"),
-                     os.path.join(INCLUDE, "tks.h")]
+SOURCES = [os.path.join(CSRC, "tks_select.cu"), os.path.join(CSRC, "tks_select512.cu"),
+           os.path.join(CSRC, "tks_order.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, "tks_device.cuh"), os.path.join(CSRC, "tks_kernel.cuh"),
+                     os.path.join(CSRC, "tks_internal.h"), os.path.join(INCLUDE, "tks.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -5,7 +5,12 @@
 
 #include <cstdint>
 
+#ifndef TKS_VARIANT
+#define TKS_VARIANT k256
+#endif
+
 namespace tks {
+namespace TKS_VARIANT {
 
 // ---------------------------------------------------------------------------
 // Shape constants
@@ -420,4 +425,5 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
   return v;
 }
 
+}  // namespace TKS_VARIANT
 }  // namespace tks

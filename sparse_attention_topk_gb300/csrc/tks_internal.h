@@ -7,6 +7,33 @@
 
 namespace tks {
 
+// Arguments of the selection kernel (both block sizes).
+struct Params {
+  const unsigned char* logits;
+  const int32_t* row_len;
+  int64_t row_stride;
+  int32_t batch;
+  int32_t k;
+  int32_t* out;
+  int32_t group;
+  int32_t test_skip_arrive;
+  unsigned char* ws;
+  int32_t slots;
+  long long spin_limit_ns;
+};
+
+// The selection kernel's launcher and set-up for each block size (256 and 512
+// threads): launch_select fills in the block size and shared memory of `base`;
+// setup_select opts in to the shared memory and reports the blocks per SM.
+namespace k256 {
+cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
+bool setup_select(int* blocks_per_sm);
+}  // namespace k256
+namespace k512 {
+cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
+bool setup_select(int* blocks_per_sm);
+}  // namespace k512
+
 // Largest k tks_topk_indices_sorted accepts: a row's k composite keys are
 // sorted in one block's shared memory.
 constexpr int kOrderKMax = 16384;

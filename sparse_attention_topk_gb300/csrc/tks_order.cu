@@ -18,6 +18,7 @@
 
 namespace tks {
 namespace {
+using namespace k256;  // key map and dependent-launch helpers
 
 constexpr int kOrderThreads = 1024;
 static_assert(kOrderKMax == TKS_SORTED_K_MAX, "the C header states the limit");

@@ -75,6 +75,9 @@ def test_options():
     assert lib.tks_set_option(tks.TKS_OPT_FORCE_GROUP, -1) == tks.TKS_E_INVAL
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
     tks.set_option(tks.TKS_OPT_SPIN_LIMIT_NS, 1_000_000_000)
+    assert lib.tks_set_option(tks.TKS_OPT_FORCE_THREADS, 384) == tks.TKS_E_INVAL
+    for t in (256, 512, 0):
+        tks.set_option(tks.TKS_OPT_FORCE_THREADS, t)
 
 
 def test_no_device_is_reported_not_faked():

@@ -64,10 +64,12 @@ def assert_matches_oracle(w, got, want=None, check_invariants=True):
 @pytest.fixture(autouse=True)
 def _defaults():
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
     tks.set_option(tks.TKS_OPT_TEST_SKIP_ARRIVE, 0)
     tks.set_option(tks.TKS_OPT_SPIN_LIMIT_NS, 1_000_000_000)
     yield
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
     tks.set_option(tks.TKS_OPT_TEST_SKIP_ARRIVE, 0)
     tks.set_option(tks.TKS_OPT_SPIN_LIMIT_NS, 1_000_000_000)
 
@@ -233,3 +235,28 @@ def test_k_larger_than_every_row_and_one_element_rows():
     assert_matches_oracle(w, run_gpu(w))
     w1 = W.from_rows("k1", [np.array([1.0, 3.0, 3.0, -0.0], np.float32)], 1)
     assert_matches_oracle(w1, run_gpu(w1))
+
+
+@pytest.mark.parametrize("threads", [256, 512])
+@pytest.mark.parametrize("name", sorted(W.NAMED))
+def test_both_block_sizes_named(threads, name):
+    """Each block size on every named workload (the automatic choice uses 512
+    only for large slices)."""
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, threads)
+    w = W.named(name)
+    assert_matches_oracle(w, run_gpu(w), oracle_of(w))
+
+
+@pytest.mark.parametrize("threads", [256, 512])
+def test_both_block_sizes_fuzz_and_splits(threads):
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, threads)
+    for w in W.fuzz_cases():
+        assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+    w = W.named("decode_128k")
+    for g in (2, 3, 16, 100):
+        tks.set_option(tks.TKS_OPT_FORCE_GROUP, g)
+        assert_matches_oracle(w, run_gpu(w), oracle_of(w))
+    tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
+    for seed in (31, 32):
+        w = W.random_rows(seed, 40, 30000, 700, levels=5)
+        assert_matches_oracle(w, run_gpu(w), check_invariants=False)
