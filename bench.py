@@ -51,6 +51,7 @@ UNIT = "us/row"
 KERNEL_SOURCES = [
     os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_select.cu"),
     os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_device.cuh"),
+    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_kernel.cuh"),
 ]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
