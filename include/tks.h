@@ -152,6 +152,12 @@ int tks_release(void);
  *   TKS_OPT_FORCE_THREADS    threads per block: 0 = automatic (512 for rows
  *                            split into slices of 48 KiB or more, else 256),
  *                            or 256 or 512
+ *   TKS_OPT_CLUSTER          rows split over one thread-block cluster, whose
+ *                            blocks merge through distributed shared memory:
+ *                            0 = automatic (rows of up to 1 MiB, about 32 KiB
+ *                            per block), 1 = never, n >= 2 = clusters of n
+ *                            blocks (at most what the device schedules) for
+ *                            every row they fit
  * Returns TKS_E_INVAL for an unknown option, a negative value or (for
  * TKS_OPT_FORCE_THREADS) a block size other than 0, 256 or 512.
  */
@@ -160,7 +166,8 @@ typedef enum {
     TKS_OPT_SPIN_LIMIT_NS = 2,
     TKS_OPT_MIN_PER_BLOCK = 3,
     TKS_OPT_TEST_SKIP_ARRIVE = 4,
-    TKS_OPT_FORCE_THREADS = 5
+    TKS_OPT_FORCE_THREADS = 5,
+    TKS_OPT_CLUSTER = 6
 } tks_option;
 int tks_set_option(int option, int64_t value);
 

@@ -39,6 +39,7 @@ TKS_OPT_SPIN_LIMIT_NS = 2
 TKS_OPT_MIN_PER_BLOCK = 3
 TKS_OPT_TEST_SKIP_ARRIVE = 4
 TKS_OPT_FORCE_THREADS = 5
+TKS_OPT_CLUSTER = 6
 
 # Every entry point include/tks.h declares, with its ctypes signature.
 _I32, _I64, _VP = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
@@ -222,5 +223,5 @@ __all__ = [
     "TKS_F32", "TKS_BF16", "TKS_OK", "TKS_E_INVAL", "TKS_E_UNSUPPORTED", "TKS_E_CUDA",
     "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_E_TOO_LARGE", "TKS_NOALLOC_MAX_ROWS",
     "TKS_K_MAX", "TKS_SORTED_K_MAX", "TKS_OPT_FORCE_GROUP",
-    "TKS_OPT_SPIN_LIMIT_NS", "TKS_OPT_MIN_PER_BLOCK", "TKS_OPT_TEST_SKIP_ARRIVE", "TKS_OPT_FORCE_THREADS",
+    "TKS_OPT_SPIN_LIMIT_NS", "TKS_OPT_MIN_PER_BLOCK", "TKS_OPT_TEST_SKIP_ARRIVE", "TKS_OPT_FORCE_THREADS", "TKS_OPT_CLUSTER",
 ]

@@ -20,18 +20,20 @@ struct Params {
   unsigned char* ws;
   int32_t slots;
   long long spin_limit_ns;
+  int32_t cluster;  // 1: each row's `group` blocks form one thread-block cluster
 };
 
 // The selection kernel's launcher and set-up for each block size (256 and 512
 // threads): launch_select fills in the block size and shared memory of `base`;
-// setup_select opts in to the shared memory and reports the blocks per SM.
+// setup_select opts in to the shared memory and to clusters of up to 16 blocks and
+// reports the blocks per SM and the largest cluster the device schedules.
 namespace k256 {
 cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
-bool setup_select(int* blocks_per_sm);
+bool setup_select(int* blocks_per_sm, int* max_cluster);
 }  // namespace k256
 namespace k512 {
 cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
-bool setup_select(int* blocks_per_sm);
+bool setup_select(int* blocks_per_sm, int* max_cluster);
 }  // namespace k512
 
 // Largest k tks_topk_indices_sorted accepts: a row's k composite keys are

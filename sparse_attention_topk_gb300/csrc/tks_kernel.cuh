@@ -338,7 +338,7 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
                                                     bool split, unsigned* g, unsigned* sync_pair,
                                                     unsigned target, bool skip_arrive,
                                                     long long limit, Ctl* ctl, unsigned* status,
-                                                    int* lo, int* hi) {
+                                                    int* lo, int* hi, unsigned* gh, bool* cl_pending) {
   constexpr int kPer = kMaxBins / kThreads;
   static_assert(kPer % 4 == 0, "bins per thread");
   const int b0 = (int)threadIdx.x * kPer;
@@ -386,6 +386,38 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
     c[j] = (b >= l && b < top) ? h[b] : 0u;
+  }
+  if (gh != nullptr) {
+    // The row is one thread-block cluster: the adds go to block 0's shared
+    // histogram gh (distributed shared memory), each returning this block's
+    // offset inside the bin; the cluster barrier replaces the L2 barrier.
+    cluster_arrive();  // every block has cleared its gh
+    cluster_wait();
+    const uint32_t g0 = dsmem_map(gh, 0u);
+    unsigned r2[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      r2[j] = c[j] ? dsmem_atom_add(g0 + 4u * (j * kThreads + threadIdx.x), c[j]) : 0u;
+    if (threadIdx.x == 0 && top > 0) dsmem_red_max(g0 + 4u * kMaxBins, (unsigned)top);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = j * kThreads + threadIdx.x;
+      if (b >= l && b < top) offs[b] = r2[j];
+    }
+    cluster_arrive();  // every block's adds are done
+    cluster_wait();
+    const int rtop = (int)min((unsigned)kMaxBins, dsmem_ld(g0 + 4u * kMaxBins));
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = j * kThreads + threadIdx.x;
+      if (b >= l && b < rtop) h[b] = dsmem_ld(g0 + 4u * b);
+    }
+    // done with block 0's words; the matching wait comes before the block exits
+    cluster_arrive();
+    *cl_pending = true;
+    __syncthreads();
+    *hi = rtop;
+    return ctl->ok != 0u;
   }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
@@ -963,7 +995,7 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
 // Returns false after an unrecoverable device-side error.
 template <int DT>
 __device__ __forceinline__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
-                           unsigned& phase_bits) {
+                           unsigned& phase_bits, bool& cl_pending) {
   using E = Elt<DT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   unsigned* h = reinterpret_cast<unsigned*>(smem + kHistOff);
@@ -990,6 +1022,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   // Valid length (clamped; a bad one is reported).
   int64_t Lr = p.row_len ? (int64_t)__ldg(p.row_len + r) : p.row_stride;
   zero_counters(h, kMaxBins);
+  // cluster rows merge into block 0's histogram in the (here unused) local
+  // candidate area: bins, then the row's top
+  unsigned* gh = p.cluster ? reinterpret_cast<unsigned*>(lcand) : nullptr;
+  if (gh != nullptr) zero_counters(gh, kMaxBins + 4);
   if (Lr < 0 || Lr > p.row_stride) {
     if (threadIdx.x == 0 && part == 0) atomicOr(status, kStatRowLen);
     Lr = Lr < 0 ? 0 : p.row_stride;
@@ -1070,7 +1106,9 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     src.visit_global(f0);
   }
   __syncthreads();
-  if (!ctl->ok) return false;
+  // (a cluster row goes through its cluster barriers even when its copy
+  // failed: the other blocks of the cluster wait for it there)
+  if (!ctl->ok && gh == nullptr) return false;
 
   // Counters of this call's parity; the other parity's are cleared below.
   const unsigned epoch = hdr.x, par = epoch & 1u;
@@ -1094,6 +1132,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   unsigned cnt = 0;
   const unsigned cap = group > 1 ? (unsigned)kGroupCandCap : (unsigned)kLocalCandCap;
   uint2* cand = group > 1 ? slot_cand : lcand;
+  unsigned nbar = 0u;  // L2 row barriers passed (each adds `group` arrivals)
   for (;;) {
     const Digit D = digit_of_round<DT>(t, pos_bits);
     const int nb = 1 << D.bits;
@@ -1112,14 +1151,16 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       const bool skip = p.test_skip_arrive && part == 0;
       if (!round0_bounds_merge(h, offs, k, group > 1, group > 1 ? slot_hist : nullptr,
                                group > 1 ? &slot->sync[par].arrive : nullptr, (unsigned)group, skip,
-                               p.spin_limit_ns, ctl, status, &lo, &hi))
+                               p.spin_limit_ns, ctl, status, &lo, &hi, gh, &cl_pending))
         return false;
+      if (gh == nullptr && group > 1) ++nbar;  // the first round's L2 barrier
       // every block of the call has read the epoch: the next call may use the other set
       if (group > 1 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
     } else if (group > 1) {
       if (!group_merge(h, offs, nb, slot_hist + (size_t)t * kMaxBins, &slot->sync[par].arrive,
-                       (unsigned)group * (t + 1), p.spin_limit_ns, ctl, status))
+                       (unsigned)group * (nbar + 1u), p.spin_limit_ns, ctl, status))
         return false;
+      ++nbar;
     }
     if (group == 1) zero_counters(offs, nb);
     unsigned bin, above;
@@ -1237,7 +1278,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     } else if (end == kEndCollect) {
       // Gather the row's candidates as they land (each slot starts as all
       // ones), put the slots back to all ones for the next call, then finish.
-      uint2* fc = reinterpret_cast<uint2*>(sl);  // this block's slice copy is no longer needed
+      // The candidates go where this block's slice copy was: every thread must
+      // be done reading it (the emission pass) first.
+      __syncthreads();
+      uint2* fc = reinterpret_cast<uint2*>(sl);
       unsigned long long* gc = reinterpret_cast<unsigned long long*>(slot_cand);
       uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
       const unsigned long long t0 = globaltimer_ns();
@@ -1318,13 +1362,16 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   grid_dependency_wait();
   __syncthreads();
   unsigned phase_bits = 0u;
+  bool cl_pending = false;  // arrived at the cluster barrier that ends block 0's reads
   if (p.group > 1) {
     const int r = blockIdx.x / p.group;
-    if (r < p.batch) select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits);
+    if (r < p.batch) select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending);
   } else {
     for (int r = blockIdx.x; r < p.batch; r += gridDim.x)
-      if (!select_row<DT>(p, r, 0, smem, phase_bits)) break;
+      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending)) break;
   }
+  // block 0 of a cluster keeps its shared memory until the others have read it
+  if (cl_pending) cluster_wait();
 }
 
 // This block size's launcher and set-up (declared in tks_internal.h).
@@ -1336,11 +1383,35 @@ cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32
                           : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
 }
 
-bool setup_select(int* blocks_per_sm) {
+bool setup_select(int* blocks_per_sm, int* max_cluster) {
   bool good = cudaFuncSetAttribute(tks_select_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemBytes) == cudaSuccess;
   good &= cudaFuncSetAttribute(tks_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes) == cudaSuccess;
+  // clusters of up to 16 blocks (one block per SM)
+  good &= cudaFuncSetAttribute(tks_select_kernel<0>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                               1) == cudaSuccess;
+  good &= cudaFuncSetAttribute(tks_select_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                               1) == cudaSuccess;
+  int c0 = 0, c1 = 0;
+  cudaLaunchConfig_t q;
+  std::memset(&q, 0, sizeof q);
+  q.gridDim = dim3(16, 1, 1);
+  q.blockDim = dim3(kThreads, 1, 1);
+  q.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute qa[1];
+  qa[0].id = cudaLaunchAttributeClusterDimension;
+  qa[0].val.clusterDim.x = 1;
+  qa[0].val.clusterDim.y = 1;
+  qa[0].val.clusterDim.z = 1;
+  q.attrs = qa;
+  q.numAttrs = 1;
+  if (cudaOccupancyMaxPotentialClusterSize(&c0, tks_select_kernel<0>, &q) != cudaSuccess ||
+      cudaOccupancyMaxPotentialClusterSize(&c1, tks_select_kernel<1>, &q) != cudaSuccess) {
+    cudaGetLastError();
+    c0 = c1 = 1;  // no clusters: rows merge through L2
+  }
+  *max_cluster = c0 < c1 ? c0 : c1;
   int b0 = 0, b1 = 0;
   good &= cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, tks_select_kernel<0>, kThreads,
                                                         kSmemBytes) == cudaSuccess;

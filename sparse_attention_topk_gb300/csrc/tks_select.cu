@@ -55,6 +55,7 @@ namespace {
 struct DeviceInfo {
   int sms = 0;
   int blocks_per_sm = 0;
+  int max_cluster = 1;  // largest thread-block cluster of the selection kernel
   bool ok = false;
 };
 
@@ -91,9 +92,10 @@ int device_info(int dev, DeviceInfo* out) {
     return TKS_E_UNSUPPORTED;
   }
   if (major == 10 && minor == 3) {
-    int b256 = 0, b512 = 0;
-    const bool good = k256::setup_select(&b256) && k512::setup_select(&b512);
+    int b256 = 0, b512 = 0, c256 = 1, c512 = 1;
+    const bool good = k256::setup_select(&b256, &c256) && k512::setup_select(&b512, &c512);
     d.blocks_per_sm = b256 < b512 ? b256 : b512;  // a plan's grid fits either block size
+    d.max_cluster = c256 < c512 ? c256 : c512;
     d.ok = good && d.blocks_per_sm >= 1;
     if (!good) cudaGetLastError();
   }
@@ -117,11 +119,47 @@ int plan_threads(int32_t batch, int64_t row_stride, int32_t dtype, int group) {
   return group > 1 && (row_stride + group - 1) / group * es >= kBigSliceBytes ? 512 : 256;
 }
 
-void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* group, int* grid) {
+// Rows up to kClusterRowBytes are split over one thread-block cluster (its
+// blocks merge through distributed shared memory and the cluster barrier)
+// with about kClusterSliceBytes per block; longer rows over more blocks
+// through L2.  TKS_OPT_CLUSTER: 0 automatic, 1 never, n >= 2 clusters of n.
+constexpr long long kClusterSliceBytes = 32 * 1024;
+std::atomic<long long> g_cluster_opt{0};
+
+int plan_cluster(const DeviceInfo& d, int32_t batch, int64_t row_stride, int32_t dtype) {
+  const long long opt = g_cluster_opt.load();
+  if (opt == 1 || g_force_group.load() > 0 || d.max_cluster < 2) return 0;
+  const long long es = dtype == TKS_F32 ? 4 : 2, bytes = row_stride * es;
+  if (row_stride <= kLoneRowMax) return 0;
+  int n;
+  if (opt >= 2) {
+    n = (int)(opt < d.max_cluster ? opt : d.max_cluster);
+  } else {
+    if (bytes > (long long)d.max_cluster * kClusterSliceBytes * 2) return 0;
+    long long want = (bytes + kClusterSliceBytes - 1) / kClusterSliceBytes;
+    if (want < 2) want = 2;
+    n = (int)(want < d.max_cluster ? want : d.max_cluster);
+  }
   const int cap = d.sms * d.blocks_per_sm;
+  if ((long long)batch * n > cap - 1) return 0;
+  if ((row_stride + n - 1) / n * es > kSliceBytes) return 0;  // slices stay on chip
+  return n;
+}
+
+void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* group, int* grid,
+                 int32_t dtype = TKS_F32, bool* cluster = nullptr) {
+  const int cap = d.sms * d.blocks_per_sm;
+  if (cluster != nullptr) *cluster = false;
   if (batch >= cap) {
     *group = 1;
     *grid = cap;
+    return;
+  }
+  const int cl = cluster != nullptr ? plan_cluster(d, batch, row_stride, dtype) : 0;
+  if (cl >= 2) {
+    *group = cl;
+    *grid = batch * cl;
+    if (cluster != nullptr) *cluster = true;
     return;
   }
   // Rows split over blocks leave one block slot of the device free when they
@@ -193,13 +231,20 @@ using namespace tks;
 // scheduled while the previous kernel of the stream finishes; it waits for it
 // before its first memory access), and a cooperative launch when the blocks of
 // a row wait for one another, so that they are all resident.
-static void set_launch_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int group) {
+static void set_launch_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int group,
+                             bool cluster = false) {
   std::memset(attr, 0, 2 * sizeof(cudaLaunchAttribute));
   int n = 0;
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
   ++n;
-  if (group > 1) {
+  if (cluster) {  // a row's blocks are one cluster, co-scheduled by construction
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)group;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  } else if (group > 1) {
     attr[n].id = cudaLaunchAttributeCooperative;
     attr[n].val.cooperative = 1;
     ++n;
@@ -236,7 +281,8 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
     if (rc != TKS_OK) return rc;
   }
   int group = 1, grid = 1;
-  plan_launch(d, batch, row_stride, &group, &grid);
+  bool cluster = false;
+  plan_launch(d, batch, row_stride, &group, &grid, dtype, &cluster);
 
   Params p;
   p.logits = static_cast<const unsigned char*>(logits);
@@ -250,13 +296,14 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
   p.ws = w.ptr;
   p.slots = w.slots;
   p.spin_limit_ns = g_spin_limit_ns.load();
+  p.cluster = cluster ? 1 : 0;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.stream = (cudaStream_t)stream;
   cudaLaunchAttribute attr[2];
-  set_launch_attrs(&cfg, attr, group);
+  set_launch_attrs(&cfg, attr, group, cluster);
   cudaError_t e = plan_threads(batch, row_stride, dtype, group) == 512
                       ? k512::launch_select(cfg, p, dtype)
                       : k256::launch_select(cfg, p, dtype);
@@ -354,6 +401,7 @@ extern "C" int tks_set_option(int option, int64_t value) {
     case TKS_OPT_SPIN_LIMIT_NS: g_spin_limit_ns.store(value > 0 ? value : 1); return TKS_OK;
     case TKS_OPT_MIN_PER_BLOCK: g_min_per_block.store(value > 0 ? value : 2048); return TKS_OK;
     case TKS_OPT_TEST_SKIP_ARRIVE: g_test_skip_arrive.store(value ? 1 : 0); return TKS_OK;
+    case TKS_OPT_CLUSTER: g_cluster_opt.store(value); return TKS_OK;
     case TKS_OPT_FORCE_THREADS:
       if (value != 0 && value != 256 && value != 512) return TKS_E_INVAL;
       g_force_threads.store(value);
@@ -378,7 +426,8 @@ extern "C" int tks_plan(int32_t batch, int64_t row_stride, int32_t k, int32_t dt
     if (rc != TKS_OK) return rc;
   }
   int g = 1, gr = 1;
-  plan_launch(d, batch, row_stride, &g, &gr);
+  bool cl = false;
+  plan_launch(d, batch, row_stride, &g, &gr, dtype, &cl);
   if (group) *group = g;
   if (grid) *grid = gr;
   return TKS_OK;
@@ -463,6 +512,7 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
   p.ws = ws;
   p.slots = TKS_NOALLOC_MAX_ROWS;
   p.spin_limit_ns = g_spin_limit_ns.load();
+  p.cluster = 0;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);

@@ -65,11 +65,13 @@ def assert_matches_oracle(w, got, want=None, check_invariants=True):
 def _defaults():
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
     tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
+    tks.set_option(tks.TKS_OPT_CLUSTER, 0)
     tks.set_option(tks.TKS_OPT_TEST_SKIP_ARRIVE, 0)
     tks.set_option(tks.TKS_OPT_SPIN_LIMIT_NS, 1_000_000_000)
     yield
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
     tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
+    tks.set_option(tks.TKS_OPT_CLUSTER, 0)
     tks.set_option(tks.TKS_OPT_TEST_SKIP_ARRIVE, 0)
     tks.set_option(tks.TKS_OPT_SPIN_LIMIT_NS, 1_000_000_000)
 
@@ -260,3 +262,42 @@ def test_both_block_sizes_fuzz_and_splits(threads):
     for seed in (31, 32):
         w = W.random_rows(seed, 40, 30000, 700, levels=5)
         assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+def test_cluster_rows(cluster):
+    """Rows split over one thread-block cluster (merge through distributed
+    shared memory) for every cluster size, and with clusters switched off."""
+    tks.set_option(tks.TKS_OPT_CLUSTER, cluster)
+    for name in ("decode_128k", "decode_4k"):
+        w = W.named(name)
+        assert_matches_oracle(w, run_gpu(w), oracle_of(w))
+    for w in W.fuzz_cases():
+        assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+    for seed in (41, 42):
+        w = W.random_rows(seed, 6, 60000, 900, levels=4)
+        assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+
+
+@pytest.mark.parametrize("threads", [256, 512])
+def test_cluster_rows_both_block_sizes_bf16(threads):
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, threads)
+    tks.set_option(tks.TKS_OPT_CLUSTER, 8)
+    rng = np.random.Generator(np.random.PCG64(43))
+    rows = [W.bf16_mixed_zeros_subnormals(rng, 150000, 0.2, 0.2, 0.2),
+            W.f32_to_bf16_bits(rng.standard_normal(70001).astype(np.float32)), W.bf16_ramp(131072)]
+    w = W.from_rows("cluster_bf16", rows, 3000, W.BF16)
+    assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+
+
+@pytest.mark.parametrize("group", [2, 3, 4])
+def test_large_slices_on_chip_finish(group):
+    """Few blocks per row, many candidates (k = 15000 among heavy ties at zero):
+    the finishing block reuses its slice buffer for the candidates, which must
+    wait until every thread has finished its emission pass over that slice."""
+    w = [x for x in W.fuzz_cases() if x.name == "bf16_zeros_subnormals"][0]
+    for threads in (256, 512):
+        tks.set_option(tks.TKS_OPT_FORCE_THREADS, threads)
+        tks.set_option(tks.TKS_OPT_FORCE_GROUP, group)
+        for _ in range(3):
+            assert_matches_oracle(w, run_gpu(w), check_invariants=False)
