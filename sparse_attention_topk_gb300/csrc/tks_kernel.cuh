@@ -391,8 +391,7 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
     // The row is one thread-block cluster: the adds go to block 0's shared
     // histogram gh (distributed shared memory), each returning this block's
     // offset inside the bin; the cluster barrier replaces the L2 barrier.
-    cluster_arrive();  // every block has cleared its gh
-    cluster_wait();
+    cluster_wait();  // every block has cleared its gh (each arrived when it did)
     const uint32_t g0 = dsmem_map(gh, 0u);
     unsigned r2[kPer];
 #pragma unroll
@@ -1025,7 +1024,14 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   // cluster rows merge into block 0's histogram in the (here unused) local
   // candidate area: bins, then the row's top
   unsigned* gh = p.cluster ? reinterpret_cast<unsigned*>(lcand) : nullptr;
-  if (gh != nullptr) zero_counters(gh, kMaxBins + 4);
+  if (gh != nullptr) {
+    zero_counters(gh, kMaxBins + 4);
+    // this block's gh is clear; the matching wait comes right before the adds,
+    // so the barrier's latency hides behind the copy and the histogram
+    __syncthreads();
+    cluster_arrive();
+    cl_pending = true;  // (consumed by the wait before the adds, or at exit)
+  }
   if (Lr < 0 || Lr > p.row_stride) {
     if (threadIdx.x == 0 && part == 0) atomicOr(status, kStatRowLen);
     Lr = Lr < 0 ? 0 : p.row_stride;
