@@ -78,12 +78,6 @@ struct SliceSrc {
   const unsigned char* sm;   // on-chip copy (resident slices)
   Slice s;
 
-  // The key of position pos of this slice (on chip when resident).
-  __device__ __forceinline__ uint32_t key_at(int pos) const {
-    using E = Elt<DT>;
-    return E::key(s.resident ? E::load(sm, pos - s.o) : E::load(row, pos));
-  }
-
   template <class F>
   __device__ __forceinline__ void vec(const uint4& x, int i0, unsigned vm, F& f) const {
     using E = Elt<DT>;

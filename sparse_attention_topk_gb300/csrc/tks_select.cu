@@ -10,23 +10,26 @@
 // obtained by extending each key with its inverted position, so the digit
 // walk simply continues into the position bits when values tie.
 //
-// Layout of the work (one kernel launch per call):
-//  * A row is split into `group` contiguous slices, one thread block (256
-//    threads, one per SM) each.  Each block copies its slice from HBM once,
-//    with bulk asynchronous copies (TMA, non-tensor form) into shared memory,
-//    and builds a 4096-bin histogram of the top 12 key bits on chip.
-//  * With group > 1 the blocks of a row add their histograms into one in L2
-//    and meet at a bounded barrier; every block then finds the threshold bin
-//    itself (the page's "TLE distributed" idea of summing block histograms
-//    and continuing with the new threshold, section "5. Triton-TLE").  The
-//    adds return each block's offset inside every bin, so each block can
-//    later write its selected positions to fixed output slots with no
-//    further coordination.
+// Layout of the work (one kernel launch per call; the kernel itself is in
+// tks_kernel.cuh, built here with 256 threads per block and in
+// tks_select512.cu with 512):
+//  * A row is split into `group` contiguous slices, one thread block (one
+//    per SM) each.  Each block copies its slice from HBM once, with a bulk
+//    asynchronous copy (TMA, non-tensor form) into shared memory, and builds
+//    a 4096-bin histogram of the top 12 key bits on chip.
+//  * With group > 1 the blocks of a row add their histograms together, in
+//    L2 behind a bounded barrier, or, when the row is one thread-block
+//    cluster, in block 0's shared memory behind cluster barriers; every
+//    block then finds the threshold bin itself (the page's "TLE distributed"
+//    idea of summing block histograms and continuing with the new threshold,
+//    section "5. Triton-TLE").  The adds return each block's offset inside
+//    every bin, so each block can later write its selected positions to
+//    fixed output slots with no further coordination.
 //  * As soon as the bin holding the k-th element has few enough members
 //    (the page's "early stop when the bucket is small", section "03."),
 //    blocks write every position above the bin to the output and push the
-//    bin's (key, position) pairs to a candidate buffer; the last block to
-//    finish refines those candidates on chip and writes the rest.
+//    bin's (key, position) pairs to a candidate buffer; block 0 of the row
+//    refines those candidates on chip and writes the rest.
 //  * With group == 1 (many rows) a block owns whole rows and needs no
 //    cross-block step at all.
 // No tensor cores: this is a streaming selection, not a contraction.
