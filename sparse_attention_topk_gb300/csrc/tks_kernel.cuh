@@ -984,11 +984,64 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   if (bad) atomicOr(status, kStatInternal);
 }
 
+// Row r's valid length, clamped into [0, row_stride] (*bad: it was not).
+__device__ __forceinline__ uint32_t row_length(const Params& p, int r, bool* bad) {
+  int64_t Lr = p.row_len ? (int64_t)__ldg(p.row_len + r) : p.row_stride;
+  *bad = Lr < 0 || Lr > p.row_stride;
+  if (*bad) Lr = Lr < 0 ? 0 : p.row_stride;
+  return (uint32_t)Lr;
+}
+
+// Block `part`'s slice of a row of L elements starting at `row`, with 16-byte
+// aligned interior boundaries.
+template <int DT>
+__device__ __forceinline__ Slice slice_geometry(uint32_t L, int part, int group,
+                                                const unsigned char* row) {
+  using E = Elt<DT>;
+  const uint32_t V = E::V;
+  const uint32_t mis = (uint32_t)(((uintptr_t)row & 15u) / E::ES);
+  auto align_up = [&](uint32_t i) -> uint32_t { return i + ((V - ((mis + i) & (V - 1u))) & (V - 1u)); };
+  auto align_down = [&](uint32_t i) -> uint32_t { return i - ((mis + i) & (V - 1u)); };
+  const uint32_t chunk = ((L + (uint32_t)group - 1u) / (uint32_t)group + V - 1u) & ~(V - 1u);
+  Slice s;
+  s.lo = part == 0 ? 0 : (int)min(L, align_up((uint32_t)part * chunk));
+  s.hi = part == group - 1 ? (int)L : (int)min(L, align_up((uint32_t)(part + 1) * chunk));
+  s.bl = (int)min((uint32_t)s.hi, align_up((uint32_t)s.lo));
+  s.bh = max(s.bl, (int)align_down((uint32_t)s.hi));
+  s.o = s.lo < s.bl ? s.bl - (int)V : s.bl;
+  s.nvec = (s.hi - s.o + (int)V - 1) / (int)V;
+  s.vb0 = s.lo < s.bl ? 1 : 0;
+  s.nbv = (s.bh - s.bl) / (int)V;
+  s.resident = s.nvec * 16 <= kSliceBytes;
+  return s;
+}
+
+// Thread 0: the bulk copies of a resident slice's whole vectors into the
+// on-chip copy, each chunk on its own mbarrier.
+template <int DT>
+__device__ __forceinline__ void issue_slice_copy(const Slice& s, const unsigned char* row,
+                                                 unsigned char* sl, Ctl* ctl) {
+  using E = Elt<DT>;
+  fence_proxy_async_smem();
+  const unsigned long long pol = policy_evict_first();
+  for (int c = 0; c < kChunks; ++c) {
+    const int c0 = s.nbv * c / kChunks, c1 = s.nbv * (c + 1) / kChunks;
+    if (c1 > c0) {
+      const unsigned bytes = (unsigned)(c1 - c0) * 16u;
+      mbar_arrive_expect_tx(&ctl->mbar[c], bytes);
+      bulk_copy_g2s(sl + (size_t)(s.vb0 + c0) * 16, row + (int64_t)s.bl * E::ES + (int64_t)c0 * 16,
+                    bytes, &ctl->mbar[c], pol);
+    }
+  }
+}
+
 // Selects the top k of row r with this block as part `part` of `group`.
-// Returns false after an unrecoverable device-side error.
+// Returns false after an unrecoverable device-side error.  copy_issued: the
+// bulk copy of this row's slice is already in flight (issued by this block at
+// the end of its previous row); on return, whether that holds for the next.
 template <int DT>
 __device__ __forceinline__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
-                           unsigned& phase_bits, bool& cl_pending) {
+                           unsigned& phase_bits, bool& cl_pending, bool& copy_issued) {
   using E = Elt<DT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   unsigned* h = reinterpret_cast<unsigned*>(smem + kHistOff);
@@ -1012,8 +1065,13 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     hdr = ld_relaxed_v4(slot);  // epoch, used[0], used[1]
   }
 
-  // Valid length (clamped; a bad one is reported).
-  int64_t Lr = p.row_len ? (int64_t)__ldg(p.row_len + r) : p.row_stride;
+  // Valid length (clamped; a bad one is reported); for a block that owns
+  // whole rows also the next row's, whose copy it issues early.
+  bool bad_len;
+  const uint32_t L = row_length(p, r, &bad_len);
+  const int r_next = r + (int)gridDim.x;
+  bool bad_next;  // (reported by the next row's own call)
+  const uint32_t L_next = group == 1 && r_next < p.batch ? row_length(p, r_next, &bad_next) : 0u;
   zero_counters(h, kMaxBins);
   // cluster rows merge into block 0's histogram in the (here unused) local
   // candidate area: bins, then the row's top
@@ -1026,11 +1084,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     cluster_arrive();
     cl_pending = true;  // (consumed by the wait before the adds, or at exit)
   }
-  if (Lr < 0 || Lr > p.row_stride) {
-    if (threadIdx.x == 0 && part == 0) atomicOr(status, kStatRowLen);
-    Lr = Lr < 0 ? 0 : p.row_stride;
-  }
-  const uint32_t L = (uint32_t)Lr;
+  if (bad_len && threadIdx.x == 0 && part == 0) atomicOr(status, kStatRowLen);
 
   // Rows with no more than k elements: every position, then -1.
   if (L <= k) {
@@ -1045,21 +1099,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
 
   // This block's slice, with 16-byte aligned interior boundaries.
   const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
-  const uint32_t V = E::V;
-  const uint32_t mis = (uint32_t)(((uintptr_t)row & 15u) / E::ES);
-  auto align_up = [&](uint32_t i) -> uint32_t { return i + ((V - ((mis + i) & (V - 1u))) & (V - 1u)); };
-  auto align_down = [&](uint32_t i) -> uint32_t { return i - ((mis + i) & (V - 1u)); };
-  const uint32_t chunk = ((L + (uint32_t)group - 1u) / (uint32_t)group + V - 1u) & ~(V - 1u);
-  Slice s;
-  s.lo = part == 0 ? 0 : (int)min(L, align_up((uint32_t)part * chunk));
-  s.hi = part == group - 1 ? (int)L : (int)min(L, align_up((uint32_t)(part + 1) * chunk));
-  s.bl = (int)min((uint32_t)s.hi, align_up((uint32_t)s.lo));
-  s.bh = max(s.bl, (int)align_down((uint32_t)s.hi));
-  s.o = s.lo < s.bl ? s.bl - (int)V : s.bl;
-  s.nvec = (s.hi - s.o + (int)V - 1) / (int)V;
-  s.vb0 = s.lo < s.bl ? 1 : 0;
-  s.nbv = (s.bh - s.bl) / (int)V;
-  s.resident = s.nvec * 16 <= kSliceBytes;
+  const Slice s = slice_geometry<DT>(L, part, group, row);
   const SliceSrc<DT> src{row, sl, s};
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
@@ -1071,19 +1111,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   };
   if (s.resident) {
     const int vb0 = s.vb0, nbv = s.nbv;
-    if (threadIdx.x == 0) {
-      fence_proxy_async_smem();
-      const unsigned long long pol = policy_evict_first();
-      for (int c = 0; c < kChunks; ++c) {
-        const int c0 = nbv * c / kChunks, c1 = nbv * (c + 1) / kChunks;
-        if (c1 > c0) {
-          const unsigned bytes = (unsigned)(c1 - c0) * 16u;
-          mbar_arrive_expect_tx(&ctl->mbar[c], bytes);
-          bulk_copy_g2s(sl + (size_t)(vb0 + c0) * 16, row + (int64_t)s.bl * E::ES + (int64_t)c0 * 16,
-                        bytes, &ctl->mbar[c], pol);
-        }
-      }
-    }
+    // (a block that owns whole rows may have issued this copy already, at the
+    // end of its previous row)
+    if (threadIdx.x == 0 && !copy_issued) issue_slice_copy<DT>(s, row, sl, ctl);
+    copy_issued = false;
     // the unaligned head and tail by plain loads
     const int nh = s.bl - s.lo, nt = s.hi - s.bh;
     if ((int)threadIdx.x < nh + nt) {
@@ -1193,6 +1224,15 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   }
 
   if (group == 1) {
+    // The slice copy is read for the last time: the next row's copy can start
+    // now and land while this row finishes.
+    const unsigned char* row_next = p.logits + (int64_t)r_next * p.row_stride * E::ES;
+    const Slice s_next = slice_geometry<DT>(L_next, 0, 1, row_next);
+    copy_issued = L_next > k && s_next.resident;
+    if (copy_issued) {
+      __syncthreads();
+      if (threadIdx.x == 0) issue_slice_copy<DT>(s_next, row_next, sl, ctl);
+    }
     if (end == kEndCollect && cnt <= kRegCandCap) {
       __syncthreads();
       uint32_t ck[kRegCand], ci[kRegCand];
@@ -1365,10 +1405,13 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   bool cl_pending = false;  // arrived at the cluster barrier that ends block 0's reads
   if (p.group > 1) {
     const int r = blockIdx.x / p.group;
-    if (r < p.batch) select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending);
+    bool copy_issued = false;
+    if (r < p.batch)
+      select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued);
   } else {
+    bool copy_issued = false;  // the next row's slice copy is in flight
     for (int r = blockIdx.x; r < p.batch; r += gridDim.x)
-      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending)) break;
+      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending, copy_issued)) break;
   }
   // block 0 of a cluster keeps its shared memory until the others have read it
   if (cl_pending) cluster_wait();

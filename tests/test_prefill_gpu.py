@@ -41,3 +41,39 @@ def test_prefill_bf16_subset():
     rows = [W.f32_to_bf16_bits(w.values[r, : w.row_len[r]]) for r in range(0, w.batch, 3)]
     wb = W.from_rows("prefill_bf16", rows, w.k, W.BF16, row_stride=w.row_stride)
     assert_matches_oracle(wb, run_gpu(wb), check_invariants=False)
+
+
+def _mixed_rows(dtype, stride, levels, seed):
+    """Rows whose lengths cycle through: empty, at most k, just above k, short,
+    resident on chip, and longer than a block's on-chip copy -- so that one
+    block's consecutive rows take every path in turn; an odd row stride gives
+    every row its own alignment."""
+    rng = np.random.default_rng(seed)
+    k = 2048
+    lens = [0, k, k + 1, 5000, stride // 3, stride, 20001, stride - 3, 77, stride // 2 + 1]
+    rows = []
+    for r in range(3 * 152 + 7):
+        n = lens[(r * 7 + r // 10) % len(lens)]
+        x = (rng.integers(0, levels, size=n).astype(np.float32) - levels / 2 if levels
+             else rng.standard_normal(n).astype(np.float32))
+        rows.append(x if dtype == W.F32 else W.f32_to_bf16_bits(x))
+    return W.from_rows(f"mixed_{dtype}_{levels}", rows, k, dtype, row_stride=stride)
+
+
+@pytest.mark.parametrize("threads", [256, 512])
+@pytest.mark.parametrize("dtype,stride", [(W.F32, 60001), (W.BF16, 100003)])
+@pytest.mark.parametrize("levels", [0, 50])
+def test_many_rows_per_block_mixed_lengths(dtype, stride, levels, threads):
+    """Each block owns several rows and starts the next row's on-chip copy
+    before finishing the current one: every combination of neighbouring row
+    kinds must still give the oracle's sets."""
+    w = _mixed_rows(dtype, stride, levels, seed=31 + levels)
+    want = oracle.topk_workload(w)
+    tks.set_option(tks.TKS_OPT_FORCE_GROUP, 1)
+    tks.set_option(tks.TKS_OPT_FORCE_THREADS, threads)
+    try:
+        assert_matches_oracle(w, run_gpu(w), want, check_invariants=False)
+        assert_matches_oracle(w, run_gpu(w, offset_elems=1), want, check_invariants=False)
+    finally:
+        tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
+        tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
