@@ -191,9 +191,32 @@ class ClockSampler:
 # the CPU oracle as baseline
 # ---------------------------------------------------------------------------
 
+class OneCore:
+    """Pins the calling thread to one host core for the duration (Linux), so
+    the single-threaded oracle timing does not migrate between cores."""
+
+    def __enter__(self):
+        self.saved = None
+        try:
+            self.saved = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {max(self.saved)})
+        except (AttributeError, OSError):
+            self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
 def cpu_oracle_time(w, budget_s: float = 10.0) -> dict:
-    """The oracle (single thread) on whole rows of the workload, repeated
-    until about budget_s of CPU work; microseconds per row."""
+    """The oracle (single thread, pinned to one core) on whole rows of the
+    workload, repeated until about budget_s of CPU work; microseconds per row."""
+    with OneCore():
+        return _cpu_oracle_time(w, budget_s)
+
+
+def _cpu_oracle_time(w, budget_s: float) -> dict:
     import oracle
     lib = oracle.load()
     times = []
@@ -211,12 +234,17 @@ def cpu_oracle_time(w, budget_s: float = 10.0) -> dict:
     return {"value": round(statistics.median(times) * 1e6, 3), "unit": UNIT, "cores": 1,
             "kind": "oracle",
             "sample": f"{r} whole rows of {w.name} (N={int(w.row_len[0])}), median of single-thread "
-                      f"C oracle runs on {os.cpu_count()} host cores (1 used)"}
+                      f"C oracle runs pinned to one of {os.cpu_count()} host cores"}
 
 
 def reference_arm(args, w):
     """--impl reference: the CPU oracle per step on a bounded prefix sample of
-    the row, scaled to a whole row by n log n."""
+    the row, scaled to a whole row by n log n (one pinned core)."""
+    with OneCore():
+        _reference_arm(args, w)
+
+
+def _reference_arm(args, w):
     import oracle
     lib = oracle.load()
     steps, warmup = args.steps, args.warmup
@@ -341,31 +369,84 @@ def gpu_arm(args, w, dist, rank, world, device):
     achieved = alg_bytes / (launch_us * 1e-6) / 1e9
     peak, peak_src = measured_peaks()
 
-    # end to end through the public API with host buffers
-    k_e2e = min(args.steps, 2000)
-    x_pin = x_host.pin_memory()
-    out_pin = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
-    x_dev = torch.empty_like(base)
-    for _ in range(3):
+    # a cold single call: before each, L2 is flushed by writing a buffer of
+    # twice its size; then one call is timed alone
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=device)
+    cold_us = []
+    for i in range(21):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            x_dev.copy_(x_pin, non_blocking=True)
+            flush.fill_(float(i))
+            c0.record(stream)
+            call(i)
+            c1.record(stream)
+        c1.synchronize()
+        cold_us.append(c0.elapsed_time(c1) * 1e3)
+    del flush
+    cold = {"us_per_call": round(statistics.median(cold_us), 3), "calls": len(cold_us),
+            "flush": f"{2 * l2 // 2**20} MiB written before each call"}
+
+    # a read-only streaming probe for context: a sum over 1 GiB
+    probe = torch.ones(2**28, dtype=torch.float32, device=device)
+    probe_ms = []
+    for _ in range(7):
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            p0.record(stream)
+            probe.sum()
+            p1.record(stream)
+        p1.synchronize()
+        probe_ms.append(p0.elapsed_time(p1))
+    del probe
+    read_probe_gbs = 2**30 / (statistics.median(probe_ms) * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: page-locked logits
+    # in, indices out, the kernel reading the logits across the host link and
+    # writing the indices back (tks_topk_indices_host); rotating host copies
+    # larger than L2 so no step is served from a cache
+    k_e2e = min(args.steps, 2000)
+    ncop_host = max(2, math.ceil(2.5 * l2 / nbytes))
+    x_pins = [x_host.pin_memory() for _ in range(ncop_host)]
+    rl_pin = None if full_rows else torch.from_numpy(w.row_len.copy()).pin_memory()
+    out_pin = torch.empty((w.batch, w.k), dtype=torch.int32).pin_memory()
+
+    def host_call(i):
+        tks.topk_indices(x_pins[i % ncop_host], w.k, row_len=rl_pin, out=out_pin, stream=stream)
+
+    def timed_e2e(step):
+        for i in range(3):
+            step(i)
+        stream.synchronize()
+        barrier(dist, device)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(k_e2e):
+            step(i)
+        f1.record(stream)
+        f1.synchronize()
+        barrier(dist, device)
+        return max_over_ranks(dist, f0.elapsed_time(f1), device) * 1e3 / (k_e2e * w.batch * world)
+
+    e2e_us_row = timed_e2e(host_call)
+    st = tks.device_status(stream)
+    if st != tks.TKS_OK:
+        raise RuntimeError(f"device status after the host-buffer run: {tks.status_string(st)}")
+    host_result = out_pin.numpy().copy()
+
+    # the same through device buffers with copy-engine copies on either side
+    x_dev = torch.empty_like(base)
+
+    def staged_call(i):
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_pins[i % ncop_host], non_blocking=True)
             tks.topk_indices(x_dev, w.k, row_len=rl, out=out, stream=stream)
             out_pin.copy_(out, non_blocking=True)
-    stream.synchronize()
-    barrier(dist, device)
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(k_e2e):
-            x_dev.copy_(x_pin, non_blocking=True)
-            tks.topk_indices(x_dev, w.k, row_len=rl, out=out, stream=stream)
-            out_pin.copy_(out, non_blocking=True)
-    f1.record(stream)
-    f1.synchronize()
-    barrier(dist, device)
-    e2e_ms = max_over_ranks(dist, f0.elapsed_time(f1), device)
-    e2e_us_row = e2e_ms * 1e3 / (k_e2e * w.batch * world)
+
+    staged_us_row = timed_e2e(staged_call)
+    del x_pins
 
     # the rank-ordered variant (tks_topk_indices_sorted: selection + on-chip
     # ordering kernel), same rotating inputs, outside the headline timing
@@ -407,13 +488,16 @@ def gpu_arm(args, w, dist, rank, world, device):
             if not np.array_equal(out_s.cpu().numpy(), oracle.topk_workload(w, ordered=True)):
                 raise RuntimeError("sorted GPU result differs from the oracle's rank order")
 
-    # the result of the last step is correct (cheap spot check on rank 0)
+    # the results of the last steps are correct (cheap spot check on rank 0)
     if rank == 0:
         import oracle
         want = oracle.topk_workload(w)
-        got = np.sort(out_pin.numpy(), axis=1)
-        if not np.array_equal(got, want):
-            raise RuntimeError("GPU result differs from the oracle")
+        for what, res in (("host-buffer", host_result), ("staged", out_pin.numpy())):
+            for r in range(w.batch):
+                take = min(w.k, int(w.row_len[r]))
+                if not (np.array_equal(np.sort(res[r, :take]), want[r, :take])
+                        and np.all(res[r, take:] == -1)):
+                    raise RuntimeError(f"{what} GPU result differs from the oracle in row {r}")
 
     if rank != 0:
         return
@@ -437,11 +521,21 @@ def gpu_arm(args, w, dist, rank, world, device):
             "frac": round(achieved / peak, 5), "peak_source": peak_src,
             "algorithmic_bytes_per_launch": alg_bytes,
             "traffic": recorded_traffic(w.name),
+            "frac_of_nominal_8000": round(achieved / 8000.0, 5),
+            "read_probe": {"gbs": round(read_probe_gbs, 1), "frac": round(achieved / read_probe_gbs, 5),
+                           "what": "torch sum over a 1 GiB fp32 buffer (library kernel, read only)"},
         },
+        "cold": cold,
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_us_row, 4), "unit": UNIT,
-                "h2d_bytes_per_step": int(nbytes), "d2h_bytes_per_step": int(w.batch * w.k * 4),
-                "steps": k_e2e},
+                "h2d_bytes_per_step": int(alg_bytes + (0 if full_rows else 4 * w.batch)),
+                "d2h_bytes_per_step": int(w.batch * w.k * 4), "steps": k_e2e,
+                "via": "tks_topk_indices_host: page-locked host logits read by the kernel, "
+                       f"indices written to page-locked host memory; {ncop_host} rotating host copies",
+                "staged_copies": {"value": round(staged_us_row, 4), "unit": UNIT,
+                                  "via": "cudaMemcpyAsync of the logits in, tks_topk_indices on "
+                                         "device buffers, cudaMemcpyAsync of the indices out",
+                                  "h2d_bytes_per_step": int(nbytes)}},
         "clocks": clk.summary(),
     }
     if sorted_line is not None:

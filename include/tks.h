@@ -98,6 +98,26 @@ int tks_topk_indices(const void *logits, const int32_t *row_len, int32_t batch,
                      void *stream);
 
 /*
+ * tks_topk_indices_host - tks_topk_indices on buffers in page-locked host
+ * memory: `logits`, `row_len` (or NULL) and `out_idx` have the layouts of
+ * tks_topk_indices but are host addresses of memory allocated with
+ * cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister on the
+ * current device's context.  The kernel reads the logits and row lengths
+ * across the host link itself (plain loads, each logit once) and writes the
+ * indices straight into `out_idx`; no copy through device memory is made.
+ *
+ * Asynchronous like tks_topk_indices: the indices are in `out_idx` once
+ * `stream` has synchronised (tks_device_status(stream) does both).  The
+ * caller must not write `logits` or `row_len`, nor read `out_idx`, until then.
+ * Returns TKS_E_INVAL, launching nothing, when a non-empty buffer is not
+ * page-locked host memory (device memory included), or on the argument
+ * errors of tks_topk_indices; otherwise as tks_topk_indices.
+ */
+int tks_topk_indices_host(const void *logits, const int32_t *row_len, int32_t batch,
+                          int64_t row_stride, int32_t k, int32_t dtype, int32_t *out_idx,
+                          void *stream);
+
+/*
  * tks_topk_indices_sorted - tks_topk_indices followed by the rank ordering of
  * each row's result: slots 0 .. min(k, len)-1 of row r hold the selected
  * positions ordered by value, largest first (+0.0 before -0.0), equal values

@@ -53,6 +53,7 @@ SIGNATURES = {
     "tks_plan": (ctypes.c_int, [_I32, _I64, _I32, _I32, _VP, _VP]),
     "tks_topk_indices_noalloc": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
     "tks_topk_indices_sorted": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
+    "tks_topk_indices_host": (ctypes.c_int, [_VP, _VP, _I32, _I64, _I32, _I32, _VP, _VP]),
 }
 
 _lock = threading.Lock()
@@ -146,6 +147,15 @@ def topk_indices_sorted_raw(logits_ptr: int, row_len_ptr: int | None, batch: int
         ctypes.c_void_p(stream_handle or 0)))
 
 
+def topk_indices_host_raw(logits_ptr: int, row_len_ptr: int | None, batch: int, row_stride: int,
+                          k: int, dtype: int, out_ptr: int, stream_handle: int | None = None) -> int:
+    """Direct call of tks_topk_indices_host (page-locked host buffers)."""
+    return int(load().tks_topk_indices_host(
+        ctypes.c_void_p(logits_ptr), ctypes.c_void_p(row_len_ptr or 0), int(batch),
+        int(row_stride), int(k), int(dtype), ctypes.c_void_p(out_ptr),
+        ctypes.c_void_p(stream_handle or 0)))
+
+
 def topk_indices_noalloc_raw(logits_ptr: int, row_len_ptr: int | None, batch: int,
                              row_stride: int, k: int, dtype: int, out_ptr: int,
                              stream_handle: int | None = None) -> int:
@@ -167,7 +177,7 @@ def _stream_handle(stream) -> int:
 
 
 def topk_indices(logits, k: int, row_len=None, out=None, stream=None, sorted: bool = False):
-    """Top-k positions of every row of a CUDA tensor.
+    """Top-k positions of every row of a CUDA tensor (or of a page-locked CPU tensor).
 
     ``logits``: float32 or bfloat16 CUDA tensor [batch, n] (or [n]) whose last
     dimension is contiguous; rows may be padded (row stride = ``logits.stride(0)``).
@@ -177,12 +187,23 @@ def topk_indices(logits, k: int, row_len=None, out=None, stream=None, sorted: bo
     tks_topk_indices_sorted, k <= TKS_SORTED_K_MAX) instead of unspecified order.
     Returns int32 [batch, k] (or [k]): each row holds its selected positions,
     then -1 where the row has fewer than k elements.
+
+    With a page-locked (pinned) CPU ``logits`` tensor, ``row_len`` and ``out``
+    are pinned CPU tensors too, the kernel reads and writes them across the
+    host link (tks_topk_indices_host, unsorted only), and the result is
+    complete once the stream has synchronised (``device_status(stream)``).
     """
     import torch
 
     squeeze = logits.dim() == 1
     x = logits.unsqueeze(0) if squeeze else logits
-    if x.dim() != 2 or not x.is_cuda:
+    host = x.dim() == 2 and not x.is_cuda
+    if host:
+        if sorted:
+            raise ValueError("rank-ordered output needs CUDA tensors")
+        if not x.is_pinned():
+            raise ValueError("CPU logits must be page-locked (tensor.pin_memory())")
+    if x.dim() != 2:
         raise ValueError("logits must be a 1-D or 2-D CUDA tensor")
     if x.dtype == torch.float32:
         dt = TKS_F32
@@ -191,34 +212,47 @@ def topk_indices(logits, k: int, row_len=None, out=None, stream=None, sorted: bo
     else:
         raise ValueError(f"unsupported dtype {x.dtype}")
     if x.size(1) > 0 and x.stride(1) != 1:
+        if host:
+            raise ValueError("CPU logits must have a contiguous last dimension")
         x = x.contiguous()
     batch, n = x.shape
     row_stride = x.stride(0) if batch > 1 else n
     if row_stride < n:
+        if host:
+            raise ValueError("CPU logits rows must not overlap")
         x = x.contiguous()
         row_stride = n
+    where = "a pinned CPU" if host else "a CUDA"
+
+    def placed(t):
+        return t.is_pinned() if host else t.is_cuda
+
     rl_ptr = None
     if row_len is not None:
-        if not (row_len.is_cuda and row_len.dtype == torch.int32 and row_len.numel() == batch):
-            raise ValueError("row_len must be an int32 CUDA tensor with one entry per row")
-        row_len = row_len.contiguous()
+        if not (placed(row_len) and row_len.dtype == torch.int32 and row_len.numel() == batch
+                and row_len.is_contiguous()):
+            raise ValueError(f"row_len must be {where} int32 tensor with one entry per row")
         rl_ptr = row_len.data_ptr()
     if out is None:
-        out = torch.empty((batch, k), dtype=torch.int32, device=x.device)
-    elif not (out.is_cuda and out.dtype == torch.int32 and out.is_contiguous()
+        out = (torch.empty((batch, k), dtype=torch.int32, pin_memory=True) if host
+               else torch.empty((batch, k), dtype=torch.int32, device=x.device))
+    elif not (placed(out) and out.dtype == torch.int32 and out.is_contiguous()
               and tuple(out.shape) == (batch, k)):
-        raise ValueError("out must be a contiguous int32 CUDA tensor [batch, k]")
-    with torch.cuda.device(x.device):
-        call = topk_indices_sorted_raw if sorted else topk_indices_raw
+        raise ValueError(f"out must be {where} contiguous int32 tensor [batch, k]")
+    device = torch.cuda.current_device() if host else x.device
+    with torch.cuda.device(device):
+        call = (topk_indices_host_raw if host else
+                topk_indices_sorted_raw if sorted else topk_indices_raw)
         rc = call(x.data_ptr() if x.numel() else 0, rl_ptr, batch,
                   row_stride if n > 0 else 0, k, dt, out.data_ptr(), _stream_handle(stream))
     if rc != TKS_OK:
-        raise TksError(rc, "tks_topk_indices_sorted" if sorted else "tks_topk_indices")
+        raise TksError(rc, "tks_topk_indices_host" if host else
+                       "tks_topk_indices_sorted" if sorted else "tks_topk_indices")
     return out[0] if squeeze else out
 
 
 __all__ = [
-    "topk_indices", "topk_indices_raw", "topk_indices_noalloc_raw", "topk_indices_sorted_raw", "device_status", "set_option", "plan", "release",
+    "topk_indices", "topk_indices_raw", "topk_indices_host_raw", "topk_indices_noalloc_raw", "topk_indices_sorted_raw", "device_status", "set_option", "plan", "release",
     "status_string", "version", "load", "lib_path", "build", "TksError", "SIGNATURES",
     "TKS_F32", "TKS_BF16", "TKS_OK", "TKS_E_INVAL", "TKS_E_UNSUPPORTED", "TKS_E_CUDA",
     "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_E_TOO_LARGE", "TKS_NOALLOC_MAX_ROWS",

@@ -77,6 +77,7 @@ struct SliceSrc {
   const unsigned char* row;  // the row in global memory
   const unsigned char* sm;   // on-chip copy (resident slices)
   Slice s;
+  bool plain;                // plain loads only (the row is in host memory)
 
   template <class F>
   __device__ __forceinline__ void vec(const uint4& x, int i0, unsigned vm, F& f) const {
@@ -126,6 +127,34 @@ struct SliceSrc {
     vec(reinterpret_cast<const uint4*>(sm)[v], i0, vm, f);
   }
 
+  // The body's whole vectors by plain loads from global memory into the
+  // on-chip copy, each counted on the way (the first pass of a row held in
+  // host memory, where bulk copies are not used).
+  template <class F>
+  __device__ __forceinline__ void load_visit_body(unsigned char* dst, F&& f) const {
+    using E = Elt<DT>;
+    const uint4* body = reinterpret_cast<const uint4*>(row + (int64_t)s.bl * E::ES);
+    uint4* out = reinterpret_cast<uint4*>(dst) + s.vb0;
+    const int nv = s.nbv;
+    constexpr int kAhead = 8;
+    for (int v0 = (int)threadIdx.x; v0 < nv; v0 += kAhead * kThreads) {
+      uint4 x[kAhead];
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a) {
+        const int v = v0 + a * kThreads;
+        x[a] = v < nv ? ld_v4(body + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a) {
+        const int v = v0 + a * kThreads;
+        if (v < nv) {
+          out[v] = x[a];
+          vec(x[a], s.bl + v * U, (1u << U) - 1u, f);
+        }
+      }
+    }
+  }
+
   // Straight from global memory (slices too large to keep on chip).
   template <class F>
   __device__ __forceinline__ void visit_global(F&& f) const {
@@ -150,7 +179,7 @@ struct SliceSrc {
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
         const int v = v0 + a * kThreads;
-        x[a] = v < nv ? ld_nc_v4(body + v) : make_uint4(0u, 0u, 0u, 0u);
+        x[a] = v >= nv ? make_uint4(0u, 0u, 0u, 0u) : plain ? ld_v4(body + v) : ld_nc_v4(body + v);
       }
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
@@ -986,7 +1015,8 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
 
 // Row r's valid length, clamped into [0, row_stride] (*bad: it was not).
 __device__ __forceinline__ uint32_t row_length(const Params& p, int r, bool* bad) {
-  int64_t Lr = p.row_len ? (int64_t)__ldg(p.row_len + r) : p.row_stride;
+  int64_t Lr = !p.row_len ? p.row_stride
+              : p.host_src ? (int64_t)ld_s32(p.row_len + r) : (int64_t)__ldg(p.row_len + r);
   *bad = Lr < 0 || Lr > p.row_stride;
   if (*bad) Lr = Lr < 0 ? 0 : p.row_stride;
   return (uint32_t)Lr;
@@ -1100,7 +1130,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   // This block's slice, with 16-byte aligned interior boundaries.
   const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
   const Slice s = slice_geometry<DT>(L, part, group, row);
-  const SliceSrc<DT> src{row, sl, s};
+  const SliceSrc<DT> src{row, sl, s, p.host_src != 0};
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
   constexpr int U = SliceSrc<DT>::U;
@@ -1109,7 +1139,17 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     for (int j = 0; j < U; ++j)
       if ((vm >> j) & 1u) atomicAdd(&h[key[j] >> E::kShift0], 1u);
   };
-  if (s.resident) {
+  if (s.resident && p.host_src) {
+    // a row in host memory: plain loads into the on-chip copy, counted as they arrive
+    const int nh = s.bl - s.lo, nt = s.hi - s.bh;
+    if ((int)threadIdx.x < nh + nt) {
+      const int i = (int)threadIdx.x < nh ? s.lo + (int)threadIdx.x : s.bh + ((int)threadIdx.x - nh);
+      E::store(sl + (size_t)(i - s.o) * E::ES, E::load(row, i));
+    }
+    src.load_visit_body(sl, f0);
+    __syncthreads();
+    src.visit_edges(f0);
+  } else if (s.resident) {
     const int vb0 = s.vb0, nbv = s.nbv;
     // (a block that owns whole rows may have issued this copy already, at the
     // end of its previous row)
@@ -1228,7 +1268,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     // now and land while this row finishes.
     const unsigned char* row_next = p.logits + (int64_t)r_next * p.row_stride * E::ES;
     const Slice s_next = slice_geometry<DT>(L_next, 0, 1, row_next);
-    copy_issued = L_next > k && s_next.resident;
+    copy_issued = !p.host_src && L_next > k && s_next.resident;
     if (copy_issued) {
       __syncthreads();
       if (threadIdx.x == 0) issue_slice_copy<DT>(s_next, row_next, sl, ctl);

@@ -256,9 +256,11 @@ static void set_launch_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
   cfg->numAttrs = (unsigned)n;
 }
 
-extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int32_t batch,
-                                int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
-                                void* stream) {
+// The selection launch behind tks_topk_indices and tks_topk_indices_host;
+// host_src: the pointers are device addresses of page-locked host memory.
+static int select_launch(const void* logits, const int32_t* row_len, int32_t batch,
+                         int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
+                         void* stream, bool host_src) {
   if (batch < 0 || row_stride < 0 || row_stride > INT32_MAX || k < 1 || k > TKS_K_MAX)
     return TKS_E_INVAL;
   if (dtype != TKS_F32 && dtype != TKS_BF16) return TKS_E_INVAL;
@@ -300,6 +302,7 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
   p.slots = w.slots;
   p.spin_limit_ns = g_spin_limit_ns.load();
   p.cluster = cluster ? 1 : 0;
+  p.host_src = host_src ? 1 : 0;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -315,6 +318,38 @@ extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int3
     return TKS_E_CUDA;
   }
   return TKS_OK;
+}
+
+extern "C" int tks_topk_indices(const void* logits, const int32_t* row_len, int32_t batch,
+                                int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
+                                void* stream) {
+  return select_launch(logits, row_len, batch, row_stride, k, dtype, out_idx, stream, false);
+}
+
+// The device address of page-locked host memory (cudaHostAlloc, cudaMallocHost
+// or cudaHostRegister), or nullptr when p is not such memory.
+static void* host_to_device(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+extern "C" int tks_topk_indices_host(const void* logits, const int32_t* row_len, int32_t batch,
+                                     int64_t row_stride, int32_t k, int32_t dtype,
+                                     int32_t* out_idx, void* stream) {
+  if (batch == 0)  // nothing is read or written: the arguments are only checked
+    return select_launch(logits, row_len, batch, row_stride, k, dtype, out_idx, stream, true);
+  if (batch < 0 || out_idx == nullptr) return TKS_E_INVAL;
+  const void* dl = row_stride > 0 && logits != nullptr ? host_to_device(logits) : nullptr;
+  void* dout = host_to_device(out_idx);
+  const void* drl = row_len != nullptr ? host_to_device(row_len) : nullptr;
+  if (dout == nullptr || (row_stride > 0 && dl == nullptr) || (row_len != nullptr && drl == nullptr))
+    return TKS_E_INVAL;
+  return select_launch(dl, static_cast<const int32_t*>(drl), batch, row_stride, k, dtype,
+                       static_cast<int32_t*>(dout), stream, true);
 }
 
 extern "C" int tks_topk_indices_sorted(const void* logits, const int32_t* row_len, int32_t batch,

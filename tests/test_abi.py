@@ -87,3 +87,15 @@ def test_no_device_is_reported_not_faked():
     # valid-looking arguments, no GPU: the library must not pretend to have run
     rc = tks.topk_indices_raw(16, None, 1, 8, 1, 0, 16, 0)
     assert rc in (tks.TKS_E_UNSUPPORTED, tks.TKS_E_CUDA)
+
+
+def test_host_entry_validates_before_any_launch():
+    assert tks.topk_indices_host_raw(16, None, -1, 8, 1, 0, 16, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_host_raw(16, None, 1, 8, 1, 0, 0, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_host_raw(0, None, 0, 8, 0, 0, 16, 0) == tks.TKS_E_INVAL
+    assert tks.topk_indices_host_raw(0, None, 0, 8, 1, 0, 16, 0) == tks.TKS_OK
+    # without a GPU (or with a pointer that is not page-locked host memory)
+    # nothing can be translated: refused, never run
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert tks.topk_indices_host_raw(16, None, 1, 8, 1, 0, 16, 0) == tks.TKS_E_INVAL
