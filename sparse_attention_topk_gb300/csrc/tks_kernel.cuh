@@ -624,9 +624,8 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
   constexpr int U = E::V;
   constexpr int B = kPassVecs;
   bool bad = false;
-  auto write = [&](uint32_t key, int pos) {
-    const uint32_t d = key >> D.shift;
-    const unsigned o = atomicAdd(&offs[d], 1u);  // rank inside the bin, row-wide
+  // an element of bin d with rank o inside the bin
+  auto place = [&](uint32_t key, int pos, uint32_t d, unsigned o) {
     if (end == kEndCollect && d == bin) {
       if (o < cap)
         put_cand(cand, o, key, pos, cand_global);
@@ -639,6 +638,10 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
       else
         bad = true;
     }
+  };
+  auto write = [&](uint32_t key, int pos) {
+    const uint32_t d = key >> D.shift;
+    place(key, pos, d, atomicAdd(&offs[d], 1u));  // rank inside the bin, row-wide
   };
   const Slice& s = src.s;
   const uint4* sv = reinterpret_cast<const uint4*>(src.sm);
@@ -660,12 +663,22 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
         sel |= (v < vb && E::key(E::lane(x[b], j)) >= t0 ? 1u : 0u) << (b * U + j);
     }
     // ... then one copy of the write path for those (rare) elements, keys
-    // re-read from shared memory, so the loop stays small
+    // re-read from shared memory, so the loop stays small; two at a time, so
+    // that two chains of (load, atomic, store) latencies overlap
     while (sel) {
-      const int q = __ffs((int)sel) - 1;
+      const int q0 = __ffs((int)sel) - 1;
       sel &= sel - 1u;
-      const int pos = s.o + (v0 + (q / U) * kThreads) * U + q % U;
-      write(E::key(E::load(src.sm, pos - s.o)), pos);  // resident: on chip
+      const int q1 = sel ? __ffs((int)sel) - 1 : -1;
+      sel &= sel - 1u;
+      const int pos0 = s.o + (v0 + (q0 / U) * kThreads) * U + q0 % U;
+      const int pos1 = s.o + (v0 + (max(q1, 0) / U) * kThreads) * U + max(q1, 0) % U;
+      const uint32_t key0 = E::key(E::load(src.sm, pos0 - s.o));  // resident: on chip
+      const uint32_t key1 = E::key(E::load(src.sm, pos1 - s.o));
+      const uint32_t d0 = key0 >> D.shift, d1 = key1 >> D.shift;
+      const unsigned o0 = atomicAdd(&offs[d0], 1u);
+      const unsigned o1 = q1 >= 0 ? atomicAdd(&offs[d1], 1u) : 0u;
+      place(key0, pos0, d0, o0);
+      if (q1 >= 0) place(key1, pos1, d1, o1);
     }
   }
   src.visit_edges([&](const uint32_t(&key)[U], const int(&pos)[U], unsigned vm) {
@@ -1065,13 +1078,19 @@ __device__ __forceinline__ void issue_slice_copy(const Slice& s, const unsigned 
   }
 }
 
+// A row length carried from one row to the next: the clamped length, bit 31
+// set when it had to be clamped; kLenUnknown when not loaded yet.
+constexpr uint32_t kLenUnknown = 0xFFFFFFFFu;
+
 // Selects the top k of row r with this block as part `part` of `group`.
 // Returns false after an unrecoverable device-side error.  copy_issued: the
 // bulk copy of this row's slice is already in flight (issued by this block at
 // the end of its previous row); on return, whether that holds for the next.
+// len_carry: row r's length if already loaded; on return, the next row's.
 template <int DT>
 __device__ __forceinline__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
-                           unsigned& phase_bits, bool& cl_pending, bool& copy_issued) {
+                                           unsigned& phase_bits, bool& cl_pending,
+                                           bool& copy_issued, uint32_t& len_carry) {
   using E = Elt<DT>;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
   unsigned* h = reinterpret_cast<unsigned*>(smem + kHistOff);
@@ -1098,10 +1117,18 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   // Valid length (clamped; a bad one is reported); for a block that owns
   // whole rows also the next row's, whose copy it issues early.
   bool bad_len;
-  const uint32_t L = row_length(p, r, &bad_len);
+  uint32_t L;
+  if (len_carry != kLenUnknown) {
+    L = len_carry & 0x7FFFFFFFu;
+    bad_len = (len_carry >> 31) != 0u;
+  } else {
+    L = row_length(p, r, &bad_len);
+  }
   const int r_next = r + (int)gridDim.x;
-  bool bad_next;  // (reported by the next row's own call)
-  const uint32_t L_next = group == 1 && r_next < p.batch ? row_length(p, r_next, &bad_next) : 0u;
+  const bool has_next = group == 1 && r_next < p.batch;
+  bool bad_next = false;  // (reported by the next row's own call)
+  const uint32_t L_next = has_next ? row_length(p, r_next, &bad_next) : 0u;
+  auto carry_next = [&] { len_carry = has_next ? (L_next | (bad_next ? 0x80000000u : 0u)) : kLenUnknown; };
   zero_counters(h, kMaxBins);
   // cluster rows merge into block 0's histogram in the (here unused) local
   // candidate area: bins, then the row's top
@@ -1120,6 +1147,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   if (L <= k) {
     for (uint32_t i = (uint32_t)part * kThreads + threadIdx.x; i < k; i += (uint32_t)kThreads * group)
       out_row[i] = i < L ? (int32_t)i : -1;
+    carry_next();
     return true;
   }
 
@@ -1269,6 +1297,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     const unsigned char* row_next = p.logits + (int64_t)r_next * p.row_stride * E::ES;
     const Slice s_next = slice_geometry<DT>(L_next, 0, 1, row_next);
     copy_issued = !p.host_src && L_next > k && s_next.resident;
+    carry_next();
     if (copy_issued) {
       __syncthreads();
       if (threadIdx.x == 0) issue_slice_copy<DT>(s_next, row_next, sl, ctl);
@@ -1446,12 +1475,15 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   if (p.group > 1) {
     const int r = blockIdx.x / p.group;
     bool copy_issued = false;
+    uint32_t len_carry = kLenUnknown;
     if (r < p.batch)
-      select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued);
+      select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued,
+                     len_carry);
   } else {
-    bool copy_issued = false;  // the next row's slice copy is in flight
+    bool copy_issued = false;          // the next row's slice copy is in flight
+    uint32_t len_carry = kLenUnknown;  // the next row's length, once loaded
     for (int r = blockIdx.x; r < p.batch; r += gridDim.x)
-      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending, copy_issued)) break;
+      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending, copy_issued, len_carry)) break;
   }
   // block 0 of a cluster keeps its shared memory until the others have read it
   if (cl_pending) cluster_wait();

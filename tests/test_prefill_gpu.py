@@ -77,3 +77,33 @@ def test_many_rows_per_block_mixed_lengths(dtype, stride, levels, threads):
     finally:
         tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
         tks.set_option(tks.TKS_OPT_FORCE_THREADS, 0)
+
+
+def test_back_to_back_batches_and_graph_replays(prefill):
+    """Blocks that own several rows each carry state from row to row (the next
+    row's length and on-chip copy): back-to-back calls of different batch
+    sizes on one stream, and replays of a captured graph, must all match."""
+    want = oracle.topk_workload(prefill)
+    s = torch.cuda.Stream()
+    x = torch.from_numpy(prefill.values.copy()).cuda()
+    rl = torch.from_numpy(prefill.row_len.copy()).cuda()
+    for batch in (prefill.batch, 153, prefill.batch, 300):
+        out = tks.topk_indices(x[:batch], prefill.k, row_len=rl[:batch], stream=s)
+        assert tks.device_status(s) == tks.TKS_OK
+        sub = W.Workload(prefill.name, prefill.values[:batch], prefill.row_len[:batch], prefill.k,
+                         prefill.dtype, "")
+        assert_matches_oracle(sub, out.cpu().numpy(), want[:batch], check_invariants=False)
+    out = torch.empty((prefill.batch, prefill.k), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(s):
+        tks.topk_indices(x, prefill.k, row_len=rl, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            tks.topk_indices(x, prefill.k, row_len=rl, out=out, stream=s)
+    for _ in range(4):
+        out.fill_(-7)
+        with torch.cuda.stream(s):
+            g.replay()
+        assert tks.device_status(s) == tks.TKS_OK
+        assert_matches_oracle(prefill, out.cpu().numpy(), want, check_invariants=False)
