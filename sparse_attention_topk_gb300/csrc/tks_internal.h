@@ -49,4 +49,14 @@ constexpr int kOrderKMax = 16384;
 cudaError_t launch_rank_order(const void* logits, int32_t batch, int64_t row_stride, int32_t k,
                               int32_t dtype, int32_t* out, cudaStream_t stream);
 
+// The same order for at most kRankMaxRows rows of k <= kRankKMax, spread over
+// many blocks: reads the unordered selection sel[batch][k] (device memory the
+// call owns, written by the kernel ahead in the stream) and writes the ordered
+// rows to out.
+constexpr int kRankMaxRows = 8;
+constexpr int kRankKMax = 4096;
+cudaError_t launch_rank_order_rows(const void* logits, int32_t batch, int64_t row_stride,
+                                   int32_t k, int32_t dtype, const int32_t* sel, int32_t* out,
+                                   cudaStream_t stream);
+
 }  // namespace tks

@@ -188,9 +188,14 @@ void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* gr
 
 int workspace_slots(const DeviceInfo& d) { return d.sms * d.blocks_per_sm; }
 
-// Layout: status header | slot headers and counters | candidate slots.
+// Layout: status header | slot headers and counters | candidate slots |
+// unordered selections of the rank-ordered path for a few rows.
+size_t workspace_rank_offset(int slots) {
+  return kWsHeaderBytes + (size_t)slots * (kSlotBytes + kCandSlotBytes);
+}
+constexpr size_t kRankScratchBytes = (size_t)kRankMaxRows * kRankKMax * sizeof(int32_t);
 size_t workspace_bytes(const DeviceInfo& d) {
-  return kWsHeaderBytes + (size_t)workspace_slots(d) * (kSlotBytes + kCandSlotBytes);
+  return workspace_rank_offset(workspace_slots(d)) + kRankScratchBytes;
 }
 
 // Counters start at zero, candidate slots at all ones ("not written").
@@ -256,11 +261,9 @@ static void set_launch_attrs(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr,
   cfg->numAttrs = (unsigned)n;
 }
 
-// The selection launch behind tks_topk_indices and tks_topk_indices_host;
-// host_src: the pointers are device addresses of page-locked host memory.
-static int select_launch(const void* logits, const int32_t* row_len, int32_t batch,
-                         int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
-                         void* stream, bool host_src) {
+// Argument checks shared by the entry points (nothing is touched on the device).
+static int check_args(const void* logits, int32_t batch, int64_t row_stride, int32_t k,
+                      int32_t dtype, const int32_t* out_idx) {
   if (batch < 0 || row_stride < 0 || row_stride > INT32_MAX || k < 1 || k > TKS_K_MAX)
     return TKS_E_INVAL;
   if (dtype != TKS_F32 && dtype != TKS_BF16) return TKS_E_INVAL;
@@ -270,6 +273,16 @@ static int select_launch(const void* logits, const int32_t* row_len, int32_t bat
   if (row_stride > 0 && (logits == nullptr || ((uintptr_t)logits % (uintptr_t)es) != 0))
     return TKS_E_INVAL;
   if ((int64_t)batch * row_stride > (INT64_MAX / 4)) return TKS_E_INVAL;
+  return TKS_OK;
+}
+
+// The selection launch behind tks_topk_indices and tks_topk_indices_host;
+// host_src: the pointers are device addresses of page-locked host memory.
+static int select_launch(const void* logits, const int32_t* row_len, int32_t batch,
+                         int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
+                         void* stream, bool host_src) {
+  const int arg = check_args(logits, batch, row_stride, k, dtype, out_idx);
+  if (arg != TKS_OK || batch == 0) return arg;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -356,6 +369,35 @@ extern "C" int tks_topk_indices_sorted(const void* logits, const int32_t* row_le
                                        int64_t row_stride, int32_t k, int32_t dtype, int32_t* out_idx,
                                        void* stream) {
   if (k > kOrderKMax) return TKS_E_INVAL;
+  if (batch >= 1 && batch <= kRankMaxRows && k <= kRankKMax) {
+    // A few rows: the selection goes to the stream's scratch, and the rank
+    // kernel writes the ordered rows to out_idx from there over many blocks.
+    const int arg = check_args(logits, batch, row_stride, k, dtype, out_idx);
+    if (arg != TKS_OK) return arg;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return TKS_E_UNSUPPORTED;
+    }
+    DeviceInfo d;
+    Workspace w;
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      int rc = device_info(dev, &d);
+      if (rc != TKS_OK) return rc;
+      rc = get_workspace(dev, stream, d, &w);
+      if (rc != TKS_OK) return rc;
+    }
+    int32_t* sel = reinterpret_cast<int32_t*>(w.ptr + workspace_rank_offset(w.slots));
+    const int rc = select_launch(logits, row_len, batch, row_stride, k, dtype, sel, stream, false);
+    if (rc != TKS_OK) return rc;
+    if (launch_rank_order_rows(logits, batch, row_stride, k, dtype, sel, out_idx,
+                               (cudaStream_t)stream) != cudaSuccess) {
+      cudaGetLastError();
+      return TKS_E_CUDA;
+    }
+    return TKS_OK;
+  }
   const int rc = tks_topk_indices(logits, row_len, batch, row_stride, k, dtype, out_idx, stream);
   if (rc != TKS_OK || batch == 0) return rc;
   if (launch_rank_order(logits, batch, row_stride, k, dtype, out_idx, (cudaStream_t)stream) !=

@@ -98,3 +98,21 @@ def test_k_above_the_sorted_limit_is_rejected():
     rc = tks.topk_indices_sorted_raw(x.data_ptr(), None, 1, 1 << 16, tks.TKS_SORTED_K_MAX + 1,
                                      tks.TKS_F32, out.data_ptr(), 0)
     assert rc == tks.TKS_E_INVAL
+
+
+@pytest.mark.parametrize("batch,k", [(1, 2048), (8, 4096), (9, 4096), (3, 4097), (5, 33)])
+def test_few_rows_over_many_blocks_and_many_rows(batch, k):
+    """Up to 8 rows with k <= 4096 are ordered over many blocks from a scratch
+    copy of the selection; more rows, or a larger k, by one block per row in
+    place.  Both sides of each limit, with ties, short rows and -inf."""
+    rng = np.random.Generator(np.random.PCG64(500 + batch * 7 + k))
+    rows = []
+    for r in range(batch):
+        n = [k // 2, k, 3 * k + 17, 20000][r % 4]
+        v = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal(n).astype(np.float32)))
+        if r % 3 == 2:
+            v[rng.integers(0, n, size=n // 5)] = -np.inf
+        rows.append(v)
+    w = W.from_rows(f"rank_{batch}_{k}", rows, k, row_stride=20011)
+    assert_same_order(w, run_sorted(w))
+    assert_same_order(w, run_sorted(w, offset_elems=1))
