@@ -128,10 +128,14 @@ int tks_topk_indices_host(const void *logits, const int32_t *row_len, int32_t ba
  *
  * Arguments, ownership, workspace and device-side errors are those of
  * tks_topk_indices, with 1 <= k <= TKS_SORTED_K_MAX (a larger k returns
- * TKS_E_INVAL and launches nothing).  Two kernels are enqueued on `stream`:
- * the selection, then one block per row that reads the row's k positions
- * and their logits and sorts them on chip; the second waits for the first.
- * Returns TKS_E_CUDA if the second launch fails (the first is enqueued).
+ * TKS_E_INVAL and launches nothing).  Two kernels are enqueued on `stream`,
+ * the second waiting for the first.  For up to 8 rows with k <= 4096 the
+ * selection is written to a scratch area of the stream's workspace, and the
+ * second kernel places every slot over many blocks (each counts, for a tile
+ * of slots, the row's selected values below each one); otherwise the
+ * selection is written to out_idx and the second kernel sorts each row in
+ * place, one block per row.  Returns TKS_E_CUDA if the second launch fails
+ * (the first is enqueued).
  */
 #define TKS_SORTED_K_MAX 16384
 int tks_topk_indices_sorted(const void *logits, const int32_t *row_len, int32_t batch,
