@@ -231,9 +231,11 @@ def _cpu_oracle_time(w, budget_s: float) -> dict:
         r += 1
         if time.perf_counter() - t_start > budget_s and r >= 3:
             break
+    lo, hi = int(w.row_len.min()), int(w.row_len.max())
+    lens = f"N={lo}" if lo == hi else f"rows taken in turn, N={lo}..{hi}"
     return {"value": round(statistics.median(times) * 1e6, 3), "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": f"{r} whole rows of {w.name} (N={int(w.row_len[0])}), median of single-thread "
+            "sample": f"{r} whole rows of {w.name} ({lens}), median of single-thread "
                       f"C oracle runs pinned to one of {os.cpu_count()} host cores"}
 
 
