@@ -289,6 +289,65 @@ def random_rows(seed: int, batch: int, max_len: int, k: int, dtype: str = F32,
     return from_rows(f"random_{seed}", rows, k, dtype, row_stride=max(1, max_len))
 
 
+def _sweep_values(rng: np.random.Generator, n: int, kind: str) -> np.ndarray:
+    """float32 values of one sweep row, by kind."""
+    if kind == "normal":
+        return rng.standard_normal(n).astype(np.float32)
+    if kind == "levels":  # heavy ties
+        return (rng.integers(0, 7, size=n).astype(np.float32) - 3.0)
+    if kind == "wide":  # many exponents, both signs
+        return (rng.choice([-1.0, 1.0], size=n) *
+                np.exp(rng.uniform(-80.0, 80.0, size=n))).astype(np.float32)
+    if kind == "specials":  # signed zeros, subnormals, -inf mixed with normals
+        v = rng.standard_normal(n).astype(np.float32)
+        m = rng.integers(0, 6, size=n)
+        v[m == 0] = 0.0
+        v[m == 1] = -0.0
+        v[m == 2] = -np.inf
+        v[m == 3] = np.float32(1e-42) * rng.integers(1, 100, size=int((m == 3).sum()))
+        return v
+    if kind == "ramp":  # sorted runs, ascending or descending
+        v = np.arange(n, dtype=np.float32)
+        return v if rng.integers(0, 2) else v[::-1].copy()
+    raise ValueError(kind)
+
+
+def sweep_cases(seed: int, count: int, max_elems: int = 2_000_000):
+    """Seeded random shapes for a parity sweep: batch, row stride, row lengths,
+    k, dtype and value kind all drawn, at most max_elems logits per case.
+    Returns (workload, draw) pairs; draw also holds the non-value choices
+    (alignment offset, block size, cluster, forced split) for the caller."""
+    rng = _rng(seed)
+    out = []
+    for c in range(count):
+        batch = int(rng.choice([1, 1, 2, 3, 5, 8, 9, 16, 64, 160, 300]))
+        cap = max(64, max_elems // batch)
+        stride = int(rng.integers(1, min(cap, 400_000) + 1))
+        ragged = bool(rng.integers(0, 2))
+        lens = rng.integers(0, stride + 1, size=batch) if ragged else np.full(batch, stride)
+        kind = str(rng.choice(["normal", "levels", "wide", "specials", "ramp"]))
+        dtype = F32 if rng.integers(0, 3) else BF16
+        kmax = int(min(TKS_K_MAX_SWEEP, max(1, stride)))
+        k = int(rng.choice([1, int(rng.integers(1, kmax + 1)), int(rng.integers(1, min(kmax, 4096) + 1)),
+                            min(kmax, 2048)]))
+        if rng.integers(0, 8) == 0:
+            k = int(min(TKS_K_MAX_SWEEP, stride + int(rng.integers(1, 50))))  # k above every length
+        rows = []
+        for r in range(batch):
+            v = _sweep_values(rng, int(lens[r]), kind)
+            rows.append(v if dtype == F32 else f32_to_bf16_bits(v))
+        w = from_rows(f"sweep{seed}_{c}", rows, max(1, k), dtype, row_stride=stride,
+                      note=f"{kind}, batch {batch}, stride {stride}, ragged {ragged}")
+        draw = {"offset": int(rng.choice([0, 0, 1, 3])), "threads": int(rng.choice([0, 256, 512])),
+                "cluster": int(rng.integers(0, 2)), "group": int(rng.choice([0, 0, 0, 2, 5, 17])),
+                "sorted": bool(rng.integers(0, 3) == 0), "host": bool(rng.integers(0, 4) == 0)}
+        out.append((w, draw))
+    return out
+
+
+TKS_K_MAX_SWEEP = 16384
+
+
 def as_float32(w: Workload) -> np.ndarray:
     """The values as float32 (bf16 widened exactly)."""
     return w.values if w.dtype == F32 else bf16_bits_to_f32(w.values)
