@@ -64,7 +64,11 @@ struct SlotHdr {
     unsigned arrive;
     unsigned top;
   } sync[2];
-  unsigned pad[8];
+  // Per parity: OR of the row's first-round keys and OR of their complements
+  // (their AND, inverted, so that both start from zero): equal iff every key
+  // of the row is the same.
+  unsigned keyset[2][2];
+  unsigned pad[4];
 };
 static_assert(sizeof(SlotHdr) == 64, "slot header is one 64-byte line");
 constexpr size_t kSlotHistOff = sizeof(SlotHdr);
@@ -86,6 +90,7 @@ struct Ctl {
   unsigned lo;                 // first-round floor bin of this block
   unsigned emit_n;             // output slots taken by the final emission
   unsigned sink;               // keeps an atomic's returned value live
+  unsigned kor, knand;         // OR of the keys and OR of their complements: block's, then row's
   unsigned red[4 * kWarps];
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block fits");

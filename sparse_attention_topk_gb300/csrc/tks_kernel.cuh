@@ -1078,6 +1078,59 @@ __device__ __forceinline__ void issue_slice_copy(const Slice& s, const unsigned 
   }
 }
 
+// The OR and the complement OR of the keys of this block's slice into
+// ctl->kor / ctl->knand (equal-as-complements iff every key is the same); for
+// a row split over blocks (keyset != nullptr) those of the whole row, through
+// the slot's key-set words and one more row barrier (bounded: on time-out
+// records the error and returns false).
+template <class Src>
+__device__ __forceinline__ bool row_key_set(const Src& src, unsigned* keyset, unsigned* arrive,
+                                            unsigned target, long long limit, Ctl* ctl,
+                                            unsigned* status) {
+  constexpr int U = Src::U;
+  if (threadIdx.x == 0) {
+    ctl->kor = 0u;
+    ctl->knand = 0u;
+  }
+  uint32_t kor = 0u, kand = ~0u;
+  src.visit([&](const uint32_t(&key)[U], const int(&)[U], unsigned vm) {
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if ((vm >> j) & 1u) {
+        kor |= key[j];
+        kand &= key[j];
+      }
+  });
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  __syncthreads();  // (the words are clear)
+  if ((threadIdx.x & 31u) == 0u) {
+    if (kor != 0u) atomicOr(&ctl->kor, kor);
+    if (~kand != 0u) atomicOr(&ctl->knand, ~kand);
+  }
+  __syncthreads();
+  if (keyset != nullptr && threadIdx.x == 0) {
+    if (ctl->kor != 0u) atomicOr(&keyset[0], ctl->kor);
+    if (ctl->knand != 0u) atomicOr(&keyset[1], ctl->knand);
+    red_release_add_u32(arrive, 1u);  // releases the two ORs
+    unsigned ok = 1u;
+    const unsigned long long t0 = globaltimer_ns();
+    while ((unsigned)ld_acquire_u64(arrive) < target) {
+      if ((long long)(globaltimer_ns() - t0) > limit) {
+        ok = 0u;
+        atomicOr(status, kStatTimeout);
+        break;
+      }
+    }
+    const unsigned long long ks = ld_relaxed_u64(reinterpret_cast<const unsigned long long*>(keyset));
+    ctl->kor = (unsigned)ks;
+    ctl->knand = (unsigned)(ks >> 32);
+    ctl->ok = ok;
+  }
+  __syncthreads();
+  return ctl->ok != 0u;
+}
+
 // A row length carried from one row to the next: the clamped length, bit 31
 // set when it had to be clamped; kLenUnknown when not loaded yet.
 constexpr uint32_t kLenUnknown = 0xFFFFFFFFu;
@@ -1255,6 +1308,23 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       if (gh == nullptr && group > 1) ++nbar;  // the first round's L2 barrier
       // every block of the call has read the epoch: the next call may use the other set
       if (group > 1 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
+      // One first-digit bin holds the whole row: if every key is the same,
+      // the answer is the k lowest positions.  Each block ORs and ANDs its
+      // keys; a split row exchanges them through the slot (one more row
+      // barrier); then each block writes its share and stops.  (Cluster rows
+      // go on with the digit rounds.)
+      if (gh == nullptr && hi > 0 && h[hi - 1] == L) {
+        if (!row_key_set(src, group > 1 ? slot->keyset[par] : nullptr,
+                         group > 1 ? &slot->sync[par].arrive : nullptr,
+                         (unsigned)group * (nbar + 1u), p.spin_limit_ns, ctl, status))
+          return false;
+        if (group > 1) ++nbar;
+        if (ctl->kor == ~ctl->knand) {
+          for (int i = s.lo + (int)threadIdx.x; i < min(s.hi, (int)k); i += kThreads) out_row[i] = i;
+          end = kEndFinal;
+          break;
+        }
+      }
     } else if (group > 1) {
       if (!group_merge(h, offs, nb, slot_hist + (size_t)t * kMaxBins, &slot->sync[par].arrive,
                        (unsigned)group * (nbar + 1u), p.spin_limit_ns, ctl, status))
@@ -1449,6 +1519,8 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (me == 0 && threadIdx.x == 0) {
       slot->sync[par ^ 1u].arrive = 0u;
       slot->sync[par ^ 1u].top = 0u;
+      slot->keyset[par ^ 1u][0] = 0u;
+      slot->keyset[par ^ 1u][1] = 0u;
     }
   }
   return true;

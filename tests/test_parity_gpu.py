@@ -301,3 +301,31 @@ def test_large_slices_on_chip_finish(group):
         tks.set_option(tks.TKS_OPT_FORCE_GROUP, group)
         for _ in range(3):
             assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+
+
+@pytest.mark.parametrize("group", [0, 1, 9])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_all_equal_rows_and_near_misses(group, dtype):
+    """A row whose keys are all equal is answered with its k lowest positions
+    right after the first round; a single differing element anywhere (higher
+    at the end, lower at the start, a -0.0 among +0.0, one ulp apart) must
+    still be found."""
+    n, k = 70001, 1500
+    base = np.full(n, 1.0, np.float32)
+    rows = [base.copy(), np.full(n, -np.inf, np.float32), np.zeros(n, np.float32)]
+    hi_end = base.copy()
+    hi_end[-1] = 2.0
+    lo_start = base.copy()
+    lo_start[0] = 0.5
+    negz = np.zeros(n, np.float32)
+    negz[123] = -0.0
+    ulp = base.copy()
+    ulp[n // 2] = np.nextafter(np.float32(1.0), np.float32(2.0)) if dtype == W.F32 else 1.0078125
+    rows += [hi_end, lo_start, negz, ulp]
+    rows = rows if dtype == W.F32 else [W.f32_to_bf16_bits(r) for r in rows]
+    w = W.from_rows(f"all_equal_{dtype}", rows, k, dtype, row_stride=n + 3)
+    tks.set_option(tks.TKS_OPT_FORCE_GROUP, group)
+    assert_matches_oracle(w, run_gpu(w), check_invariants=False)
+    assert_matches_oracle(w, run_gpu(w, offset_elems=1), check_invariants=False)
+    tks.set_option(tks.TKS_OPT_CLUSTER, 1)
+    assert_matches_oracle(w, run_gpu(w), check_invariants=False)
