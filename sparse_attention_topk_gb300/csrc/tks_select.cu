@@ -32,6 +32,8 @@
 //    refines those candidates on chip and writes the rest.
 //  * With group == 1 (many rows) a block owns whole rows and needs no
 //    cross-block step at all.
+//  * A row whose keys are all equal (a constant row, all -inf) is answered
+//    right after the first round with its lowest positions.
 // No tensor cores: this is a streaming selection, not a contraction.
 
 #include <cuda_runtime.h>
