@@ -22,7 +22,6 @@ NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-    "-shared",
 ]
 
 
@@ -45,12 +44,28 @@ def build(force: bool = False, verbose_ptxas: bool = False, out: str = LIB_PATH)
     if not force and out == LIB_PATH and up_to_date(out):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
-    tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_FLAGS, f"-I{INCLUDE}", f"-I{CSRC}", *SOURCES, "-o", tmp]
-    if verbose_ptxas:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, out)
+    tag = f".tmp{os.getpid()}"
+    nvcc = nvcc_path()
+    # one process per translation unit, in parallel, then one link
+    objs = [os.path.join(os.path.dirname(out), os.path.basename(src) + tag + ".o") for src in SOURCES]
+    procs = []
+    for src, obj in zip(SOURCES, objs):
+        cmd = [nvcc, *NVCC_FLAGS, f"-I{INCLUDE}", f"-I{CSRC}", "-c", src, "-o", obj]
+        if verbose_ptxas:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((src, subprocess.Popen(cmd)))
+    failed = [src for src, pr in procs if pr.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, f"nvcc -c {' '.join(failed)}")
+        tmp = out + tag
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs,
+                        "-o", tmp], check=True)
+        os.replace(tmp, out)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return out
 
 
