@@ -58,6 +58,24 @@ def test_invalid_arguments_rejected_before_any_cuda_call(args):
     assert tks.topk_indices_raw(logits, row_len, batch, stride, k, dtype, out, 0) == tks.TKS_E_INVAL
 
 
+@pytest.mark.parametrize("args", [
+    # logits, row_len, batch, row_stride, k, dtype, out -- a few rows and k <= 4096 (the
+    # many-block ordering path) and more rows (the one-block path) alike
+    (16, None, 1, 8, 0, 0, 16),
+    (16, None, 2, 8, 1, 7, 16),
+    (16, None, 3, 8, 1, 0, 0),
+    (16, None, 3, 8, 1, 0, 18),
+    (0, None, 1, 8, 1, 0, 16),
+    (18, None, 1, 8, 1, 0, 16),
+    (16, None, 9, -8, 1, 0, 16),
+    (16, None, 20, 8, 0, 0, 16),
+])
+def test_sorted_entry_rejects_bad_arguments_before_any_cuda_call(args):
+    logits, row_len, batch, stride, k, dtype, out = args
+    assert tks.topk_indices_sorted_raw(logits, row_len, batch, stride, k, dtype, out, 0) == \
+        tks.TKS_E_INVAL
+
+
 def test_sorted_entry_validates_like_the_plain_one():
     assert tks.topk_indices_sorted_raw(16, None, 1, 8, tks.TKS_SORTED_K_MAX + 1, 0, 16, 0) == tks.TKS_E_INVAL
     assert tks.topk_indices_sorted_raw(16, None, 1, 8, 0, 0, 16, 0) == tks.TKS_E_INVAL
