@@ -542,7 +542,7 @@ def gpu_arm(args, w, dist, rank, world, device):
     }
     if sorted_line is not None:
         line["sorted"] = sorted_line
-    if rank == 0 and world >= 1:
+    if rank == 0 and world == 1:  # (the CPU baseline is taken at N=1 only)
         line["cpu_baseline"] = cpu_oracle_time(w, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
 
