@@ -29,11 +29,13 @@ struct Params {
 // setup_select opts in to the shared memory and to clusters of up to 16 blocks and
 // reports the blocks per SM and the largest cluster the device schedules.
 namespace k256 {
-cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
+cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype,
+                          bool lean);
 bool setup_select(int* blocks_per_sm, int* max_cluster);
 }  // namespace k256
 namespace k512 {
-cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype);
+cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype,
+                          bool lean);
 bool setup_select(int* blocks_per_sm, int* max_cluster);
 }  // namespace k512
 

@@ -1140,7 +1140,9 @@ constexpr uint32_t kLenUnknown = 0xFFFFFFFFu;
 // bulk copy of this row's slice is already in flight (issued by this block at
 // the end of its previous row); on return, whether that holds for the next.
 // len_carry: row r's length if already loaded; on return, the next row's.
-template <int DT>
+// kLean: a row split over blocks whose slices all fit on chip, logits in
+// device memory, no cluster -- the other paths are not compiled in.
+template <int DT, bool kLean>
 __device__ __forceinline__ bool select_row(const Params& p, int r, int part, unsigned char* smem,
                                            unsigned& phase_bits, bool& cl_pending,
                                            bool& copy_issued, uint32_t& len_carry) {
@@ -1185,7 +1187,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   zero_counters(h, kMaxBins);
   // cluster rows merge into block 0's histogram in the (here unused) local
   // candidate area: bins, then the row's top
-  unsigned* gh = p.cluster ? reinterpret_cast<unsigned*>(lcand) : nullptr;
+  unsigned* gh = !kLean && p.cluster ? reinterpret_cast<unsigned*>(lcand) : nullptr;
   if (gh != nullptr) {
     zero_counters(gh, kMaxBins + 4);
     // this block's gh is clear; the matching wait comes right before the adds,
@@ -1220,7 +1222,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     for (int j = 0; j < U; ++j)
       if ((vm >> j) & 1u) atomicAdd(&h[key[j] >> E::kShift0], 1u);
   };
-  if (s.resident && p.host_src) {
+  if (!kLean && s.resident && p.host_src) {
     // a row in host memory: plain loads into the on-chip copy, counted as they arrive
     const int nh = s.bl - s.lo, nt = s.hi - s.bh;
     if ((int)threadIdx.x < nh + nt) {
@@ -1230,7 +1232,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     src.load_visit_body(sl, f0);
     __syncthreads();
     src.visit_edges(f0);
-  } else if (s.resident) {
+  } else if (kLean || s.resident) {
     const int vb0 = s.vb0, nbv = s.nbv;
     // (a block that owns whole rows may have issued this copy already, at the
     // end of its previous row)
@@ -1291,7 +1293,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (t > 0) {
       zero_counters(h, nb);
       __syncthreads();
-      if (s.resident)
+      if (kLean || s.resident)
         later_pass_resident<DT, false>(src, P, D, pmax, h, 0u, 0, 0u, nullptr, nullptr, nullptr, 0u,
                                        nullptr, false, 0u, status);
       else
@@ -1340,10 +1342,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     // anywhere in the row, has nothing to emit)
     if (end != kEndAbove || above != 0u) {
       const uint32_t t0 = (end == kEndAbove ? bin + 1u : bin) << D.shift;
-      if (t == 0 && s.resident && !(end == kEndAbove && t0 == 0u))
+      if (t == 0 && (kLean || s.resident) && !(end == kEndAbove && t0 == 0u))
         emit_first_resident(src, t0, D, bin, end, base, h, offs, out_row, k, cand, group > 1, cap,
                             status);
-      else if (s.resident)
+      else if (kLean || s.resident)
         later_pass_resident<DT, true>(src, P, D, pmax, nullptr, bin, end, base, h, offs, out_row, k,
                                       cand, group > 1, cap, status);
       else
@@ -1361,7 +1363,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     }
   }
 
-  if (group == 1) {
+  if (!kLean && group == 1) {
     // The slice copy is read for the last time: the next row's copy can start
     // now and land while this row finishes.
     const unsigned char* row_next = p.logits + (int64_t)r_next * p.row_stride * E::ES;
@@ -1526,7 +1528,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   return true;
 }
 
-template <int DT>
+template <int DT, bool kLean>
 __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + kCtlOff);
@@ -1544,41 +1546,50 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   __syncthreads();
   unsigned phase_bits = 0u;
   bool cl_pending = false;  // arrived at the cluster barrier that ends block 0's reads
-  if (p.group > 1) {
+  if (kLean || p.group > 1) {
     const int r = blockIdx.x / p.group;
     bool copy_issued = false;
     uint32_t len_carry = kLenUnknown;
     if (r < p.batch)
-      select_row<DT>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued,
-                     len_carry);
+      select_row<DT, kLean>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued,
+                            len_carry);
   } else {
     bool copy_issued = false;          // the next row's slice copy is in flight
     uint32_t len_carry = kLenUnknown;  // the next row's length, once loaded
     for (int r = blockIdx.x; r < p.batch; r += gridDim.x)
-      if (!select_row<DT>(p, r, 0, smem, phase_bits, cl_pending, copy_issued, len_carry)) break;
+      if (!select_row<DT, kLean>(p, r, 0, smem, phase_bits, cl_pending, copy_issued, len_carry))
+        break;
   }
   // block 0 of a cluster keeps its shared memory until the others have read it
   if (cl_pending) cluster_wait();
 }
 
 // This block size's launcher and set-up (declared in tks_internal.h).
-cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype) {
+cudaError_t launch_select(const cudaLaunchConfig_t& base, const Params& p, int32_t dtype,
+                          bool lean) {
   cudaLaunchConfig_t cfg = base;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
-  return dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0>, p)
-                          : cudaLaunchKernelEx(&cfg, tks_select_kernel<1>, p);
+  if (lean)
+    return dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0, true>, p)
+                            : cudaLaunchKernelEx(&cfg, tks_select_kernel<1, true>, p);
+  return dtype == TKS_F32 ? cudaLaunchKernelEx(&cfg, tks_select_kernel<0, false>, p)
+                          : cudaLaunchKernelEx(&cfg, tks_select_kernel<1, false>, p);
 }
 
 bool setup_select(int* blocks_per_sm, int* max_cluster) {
-  bool good = cudaFuncSetAttribute(tks_select_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  bool good = cudaFuncSetAttribute(tks_select_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSmemBytes) == cudaSuccess;
-  good &= cudaFuncSetAttribute(tks_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  good &= cudaFuncSetAttribute(tks_select_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes) == cudaSuccess;
+  good &= cudaFuncSetAttribute(tks_select_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes) == cudaSuccess;
+  good &= cudaFuncSetAttribute(tks_select_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes) == cudaSuccess;
   // clusters of up to 16 blocks (one block per SM)
-  good &= cudaFuncSetAttribute(tks_select_kernel<0>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+  good &= cudaFuncSetAttribute(tks_select_kernel<0, false>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                1) == cudaSuccess;
-  good &= cudaFuncSetAttribute(tks_select_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+  good &= cudaFuncSetAttribute(tks_select_kernel<1, false>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                1) == cudaSuccess;
   int c0 = 0, c1 = 0;
   cudaLaunchConfig_t q;
@@ -1593,16 +1604,16 @@ bool setup_select(int* blocks_per_sm, int* max_cluster) {
   qa[0].val.clusterDim.z = 1;
   q.attrs = qa;
   q.numAttrs = 1;
-  if (cudaOccupancyMaxPotentialClusterSize(&c0, tks_select_kernel<0>, &q) != cudaSuccess ||
-      cudaOccupancyMaxPotentialClusterSize(&c1, tks_select_kernel<1>, &q) != cudaSuccess) {
+  if (cudaOccupancyMaxPotentialClusterSize(&c0, tks_select_kernel<0, false>, &q) != cudaSuccess ||
+      cudaOccupancyMaxPotentialClusterSize(&c1, tks_select_kernel<1, false>, &q) != cudaSuccess) {
     cudaGetLastError();
     c0 = c1 = 1;  // no clusters: rows merge through L2
   }
   *max_cluster = c0 < c1 ? c0 : c1;
   int b0 = 0, b1 = 0;
-  good &= cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, tks_select_kernel<0>, kThreads,
+  good &= cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, tks_select_kernel<0, false>, kThreads,
                                                         kSmemBytes) == cudaSuccess;
-  good &= cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, tks_select_kernel<1>, kThreads,
+  good &= cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, tks_select_kernel<1, false>, kThreads,
                                                         kSmemBytes) == cudaSuccess;
   *blocks_per_sm = b0 < b1 ? b0 : b1;
   return good;

@@ -190,6 +190,16 @@ void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* gr
 
 int workspace_slots(const DeviceInfo& d) { return d.sms * d.blocks_per_sm; }
 
+// Whether every block's slice of a row of up to row_stride elements split
+// over `group` blocks fits the on-chip copy (its 16-byte vectors, with one
+// partial vector at each end), so the kernel without the streamed path may
+// be used.
+bool slices_fit_on_chip(int64_t row_stride, int group, int32_t dtype) {
+  const int64_t es = dtype == TKS_F32 ? 4 : 2, v = 16 / es;
+  const int64_t chunk = ((row_stride + group - 1) / group + v - 1) / v * v;
+  return (chunk / v + 2) * 16 <= (int64_t)kSliceBytes;
+}
+
 // Layout: status header | slot headers and counters | candidate slots |
 // unordered selections of the rank-ordered path for a few rows.
 size_t workspace_rank_offset(int slots) {
@@ -304,7 +314,7 @@ static int select_launch(const void* logits, const int32_t* row_len, int32_t bat
   bool cluster = false;
   plan_launch(d, batch, row_stride, &group, &grid, dtype, &cluster);
 
-  Params p;
+  Params p{};
   p.logits = static_cast<const unsigned char*>(logits);
   p.row_len = row_len;
   p.row_stride = row_stride;
@@ -318,6 +328,8 @@ static int select_launch(const void* logits, const int32_t* row_len, int32_t bat
   p.spin_limit_ns = g_spin_limit_ns.load();
   p.cluster = cluster ? 1 : 0;
   p.host_src = host_src ? 1 : 0;
+  // (the kernel without the streamed, host-memory, cluster and whole-row paths)
+  const bool lean = group > 1 && !cluster && !host_src && slices_fit_on_chip(row_stride, group, dtype);
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -326,8 +338,8 @@ static int select_launch(const void* logits, const int32_t* row_len, int32_t bat
   cudaLaunchAttribute attr[2];
   set_launch_attrs(&cfg, attr, group, cluster);
   cudaError_t e = plan_threads(batch, row_stride, dtype, group) == 512
-                      ? k512::launch_select(cfg, p, dtype)
-                      : k256::launch_select(cfg, p, dtype);
+                      ? k512::launch_select(cfg, p, dtype, lean)
+                      : k256::launch_select(cfg, p, dtype, lean);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return TKS_E_CUDA;
@@ -582,7 +594,7 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
     return TKS_E_CUDA;
   }
 
-  Params p;
+  Params p{};
   p.logits = static_cast<const unsigned char*>(logits);
   p.row_len = row_len;
   p.row_stride = row_stride;
@@ -595,6 +607,8 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
   p.slots = TKS_NOALLOC_MAX_ROWS;
   p.spin_limit_ns = g_spin_limit_ns.load();
   p.cluster = 0;
+  p.host_src = 0;
+  const bool lean = group > 1 && slices_fit_on_chip(row_stride, group, dtype);
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -603,8 +617,8 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
   cudaLaunchAttribute attr[2];
   set_launch_attrs(&cfg, attr, group);
   const cudaError_t e = plan_threads(batch, row_stride, dtype, group) == 512
-                            ? k512::launch_select(cfg, p, dtype)
-                            : k256::launch_select(cfg, p, dtype);
+                            ? k512::launch_select(cfg, p, dtype, lean)
+                            : k256::launch_select(cfg, p, dtype, lean);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return TKS_E_CUDA;
