@@ -98,8 +98,9 @@ int tks_topk_indices(const void *logits, const int32_t *row_len, int32_t batch,
                      void *stream);
 
 /*
- * tks_topk_indices_host - tks_topk_indices on buffers in page-locked host
- * memory: `logits`, `row_len` (or NULL) and `out_idx` have the layouts of
+ * tks_topk_indices_host - tks_topk_indices (the operation defined at the top
+ * of this file) on buffers in page-locked host memory, for callers whose
+ * logits are on the host: `logits`, `row_len` (or NULL) and `out_idx` have the layouts of
  * tks_topk_indices but are host addresses of memory allocated with
  * cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister on the
  * current device's context.  The kernel reads the logits and row lengths
