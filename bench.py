@@ -48,11 +48,12 @@ import workloads as W  # noqa: E402
 
 METRIC = "TopK-select µs/row and HBM GB/s (batch=1, N=128K–1M, k=2048) vs roofline"
 UNIT = "us/row"
+# every file that is compiled into libtks.so
 KERNEL_SOURCES = [
-    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_select.cu"),
-    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_device.cuh"),
-    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", "tks_kernel.cuh"),
-]
+    os.path.join(ROOT, "sparse_attention_topk_gb300", "csrc", name)
+    for name in ("tks_select.cu", "tks_select512.cu", "tks_order.cu", "tks_device.cuh",
+                 "tks_kernel.cuh", "tks_internal.h")
+] + [os.path.join(ROOT, "include", "tks.h")]
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -285,6 +286,179 @@ def _reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+
+# ---------------------------------------------------------------------------
+# device timing of one workload
+# ---------------------------------------------------------------------------
+
+class DeviceTiming:
+    """Back-to-back and cold timing of tks_topk_indices on one workload.
+
+    Steps read rotating copies of the input whose total size exceeds 2.5x the
+    L2 cache; L2 is flushed just before the timed region and a copy is read
+    again only after all the others, so every step reads its logits from HBM.
+    Steps are captured in CUDA graphs of up to 512 calls (graph j reads the
+    copies from j * 512 on); the warm-up replays each graph the timed region
+    uses at least once (a graph's first launch uploads it), and a short spin
+    kernel ahead of the first event keeps the device busy while the host
+    submits the graphs, so the timed region holds the K calls and nothing else.
+    """
+
+    SPIN_CYCLES = 200_000  # ~0.1 ms at the GB300's clocks
+
+    def __init__(self, tks, torch, w, stream, device, l2):
+        self.tks, self.torch, self.w, self.stream, self.device, self.l2 = tks, torch, w, stream, device, l2
+        x_host = torch.from_numpy(w.values.copy())
+        if w.dtype == W.BF16:
+            x_host = x_host.view(torch.bfloat16)
+        self.x_host = x_host
+        self.nbytes = x_host.numel() * x_host.element_size()
+        self.ncopies = max(2, math.ceil(2.5 * l2 / self.nbytes))
+        self.base = x_host.to(device)
+        self.copies = [self.base.clone() for _ in range(self.ncopies)]
+        self.full_rows = bool(np.all(w.row_len == w.row_stride))
+        self.rl = None if self.full_rows else torch.from_numpy(w.row_len.copy()).to(device)
+        self.out = torch.empty((w.batch, w.k), dtype=torch.int32, device=device)
+        self.flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=device)
+        self.graphs = {}
+        self.G = 1
+        with torch.cuda.stream(stream):
+            self.call(0)  # sets up the stream's workspace before capture
+        stream.synchronize()
+        st = tks.device_status(stream)
+        if st != tks.TKS_OK:
+            raise RuntimeError(f"device status after set-up: {tks.status_string(st)}")
+
+    def call(self, i):
+        self.tks.topk_indices(self.copies[i % self.ncopies], self.w.k, row_len=self.rl, out=self.out,
+                              stream=self.stream)
+
+    def graph_calls(self, steps):
+        self.G = min(512, max(1, steps))
+        return self.G
+
+    def _keys(self, k):
+        """(calls, first copy) of the graphs that run k steps."""
+        n_off = 1 if self.ncopies <= self.G else math.ceil(self.ncopies / self.G)
+        keys, j = [], 0
+        while k > 0:
+            n = min(self.G, k)
+            keys.append((n, (j % n_off) * self.G))
+            k -= n
+            j += 1
+        return keys
+
+    def _graph(self, key):
+        if key not in self.graphs:
+            torch = self.torch
+            n, off = key
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(n):
+                    self.call(off + i)
+            self.graphs[key] = g
+        return self.graphs[key]
+
+    def run(self, k):
+        with self.torch.cuda.stream(self.stream):
+            for key in self._keys(k):
+                self._graph(key).replay()
+
+    def warm(self, steps, warmup):
+        """Replays every graph that run(steps) uses once, then more steps up to
+        `warmup` in all; returns the number of warm-up steps made."""
+        done = 0
+        with self.torch.cuda.stream(self.stream):
+            for key in dict.fromkeys(self._keys(steps)):
+                self._graph(key).replay()
+                done += key[0]
+        if done < max(3, warmup):
+            self.run(max(3, warmup) - done)
+            done = max(3, warmup)
+        self.stream.synchronize()
+        return done
+
+    def timed(self, steps):
+        """Device time of exactly `steps` calls (ms), CUDA events on the stream."""
+        torch = self.torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            self.flush.fill_(1.0)
+            torch.cuda._sleep(self.SPIN_CYCLES)
+            e0.record(self.stream)
+        self.run(steps)
+        e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
+    def cold(self, calls=21):
+        """One call after L2 has been flushed by writing twice its size, timed
+        alone (no earlier call to overlap with); median over `calls`."""
+        torch = self.torch
+        flush = self.flush
+        cold_us = []
+        for i in range(calls):
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                flush.fill_(float(i))
+                c0.record(self.stream)
+                self.call(i)
+                c1.record(self.stream)
+            c1.synchronize()
+            cold_us.append(c0.elapsed_time(c1) * 1e3)
+        st = self.tks.device_status(self.stream)
+        if st != self.tks.TKS_OK:
+            raise RuntimeError(f"device status after the cold calls: {self.tks.status_string(st)}")
+        return {"us_per_call": round(statistics.median(cold_us), 3), "calls": len(cold_us),
+                "flush": f"{2 * self.l2 // 2**20} MiB written before each call"}
+
+    def release(self):
+        self.graphs.clear()
+        self.copies = []
+        self.flush = None
+
+
+def other_configs(tks, torch, args, main_name, stream, device, l2, peak, gpu_id):
+    """µs per row, GB/s, fraction of peak and cold latency of the other named
+    workloads, each timed like the headline (back to back in CUDA graphs over
+    rotating copies larger than L2) and checked against the oracle."""
+    import oracle
+    res = {}
+    steps = max(3, min(args.steps, 2048))
+    with ClockSampler(gpu_id) as clk:
+        for name in W.NAMED:
+            if name == main_name:
+                continue
+            w = W.named(name)
+            dev = DeviceTiming(tks, torch, w, stream, device, l2)
+            dev.graph_calls(steps)
+            dev.warm(steps, args.warmup)
+            ms = dev.timed(steps)
+            st = tks.device_status(stream)
+            if st != tks.TKS_OK:
+                raise RuntimeError(f"{name}: device status {tks.status_string(st)}")
+            got = dev.out.cpu().numpy()
+            want = oracle.topk_workload(w)
+            ok = all(np.array_equal(np.sort(got[r, :min(w.k, int(w.row_len[r]))]),
+                                    want[r, :min(w.k, int(w.row_len[r]))]) for r in range(w.batch))
+            if not ok:
+                raise RuntimeError(f"{name}: GPU result differs from the oracle")
+            us_call = ms * 1e3 / steps
+            gbs = w.algorithmic_bytes / (us_call * 1e-6) / 1e9
+            res[name] = {"us_per_row": round(us_call / w.batch, 4), "us_per_call": round(us_call, 3),
+                         "batch": w.batch, "n": int(w.row_stride), "k": w.k, "logits": w.dtype,
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 5), "steps": steps,
+                         "cold_us_per_call": dev.cold(11)["us_per_call"], "matches_oracle": True,
+                         "plan": dict(zip(("blocks_per_row", "grid"),
+                                          tks.plan(w.batch, w.row_stride, w.k, 0 if w.dtype == W.F32 else 1)))}
+            dev.release()
+            del dev
+            torch.cuda.empty_cache()
+    res["clocks"] = clk.summary()
+    return res
+
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
@@ -299,70 +473,26 @@ def gpu_arm(args, w, dist, rank, world, device):
     stream = torch.cuda.Stream(device)
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
-    x_host = torch.from_numpy(w.values.copy())
-    if w.dtype == W.BF16:
-        x_host = x_host.view(torch.bfloat16)
-    nbytes = x_host.numel() * x_host.element_size()
-    ncopies = max(2, math.ceil(2.5 * l2 / nbytes))
-    base = x_host.to(device)
-    copies = [base.clone() for _ in range(ncopies)]
-    full_rows = bool(np.all(w.row_len == w.row_stride))
-    rl = None if full_rows else torch.from_numpy(w.row_len.copy()).to(device)
-    out = torch.empty((w.batch, w.k), dtype=torch.int32, device=device)
-
-    def call(i):
-        tks.topk_indices(copies[i % ncopies], w.k, row_len=rl, out=out, stream=stream)
-
-    with torch.cuda.stream(stream):
-        call(0)  # sets up the stream's workspace before capture
-    stream.synchronize()
-    st = tks.device_status(stream)
-    if st != tks.TKS_OK:
-        raise RuntimeError(f"device status after set-up: {tks.status_string(st)}")
-
-    G = min(512, args.steps)
-
-    def capture(n, offset):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                call(offset + i)
-        return g
-
-    g_full = capture(G, 0)
-    tail = args.steps % G
-    g_tail = capture(tail, 0) if tail else None
-
-    def run_steps(k):
-        with torch.cuda.stream(stream):
-            for _ in range(k // G):
-                g_full.replay()
-            if k % G:
-                (g_tail if k % G == tail and g_tail is not None else capture(k % G, 0)).replay()
-
-    # warm-up: W steps
-    run_steps(max(3, args.warmup))
-    stream.synchronize()
+    dev = DeviceTiming(tks, torch, w, stream, device, l2)
+    x_host, nbytes, ncopies = dev.x_host, dev.nbytes, dev.ncopies
+    copies, out, rl, full_rows, base = dev.copies, dev.out, dev.rl, dev.full_rows, dev.base
+    G = dev.graph_calls(args.steps)
+    warm_steps = dev.warm(args.steps, args.warmup)
 
     # timed: exactly K steps
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize(device)
     uuid = getattr(props, "uuid", None)
     gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else str(uuid or device.index)
     with ClockSampler(gpu_id) as clk:
-        e0.record(stream)
-        run_steps(args.steps)
-        e1.record(stream)
-        e1.synchronize()
+        ms = dev.timed(args.steps)
     torch.cuda.synchronize(device)
     barrier(dist, device)
-    ms = e0.elapsed_time(e1)
     st = tks.device_status(stream)
     if st != tks.TKS_OK:
         raise RuntimeError(f"device status after the timed run: {tks.status_string(st)}")
     ms_max = max_over_ranks(dist, ms, device)
+    call = dev.call
 
     rows_total = args.steps * w.batch * world
     us_per_row = ms_max * 1e3 / rows_total
@@ -371,23 +501,7 @@ def gpu_arm(args, w, dist, rank, world, device):
     achieved = alg_bytes / (launch_us * 1e-6) / 1e9
     peak, peak_src = measured_peaks()
 
-    # a cold single call: before each, L2 is flushed by writing a buffer of
-    # twice its size; then one call is timed alone
-    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=device)
-    cold_us = []
-    for i in range(21):
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            flush.fill_(float(i))
-            c0.record(stream)
-            call(i)
-            c1.record(stream)
-        c1.synchronize()
-        cold_us.append(c0.elapsed_time(c1) * 1e3)
-    del flush
-    cold = {"us_per_call": round(statistics.median(cold_us), 3), "calls": len(cold_us),
-            "flush": f"{2 * l2 // 2**20} MiB written before each call"}
+    cold = dev.cold()
 
     # a read-only streaming probe for context: a sum over 1 GiB
     probe = torch.ones(2**28, dtype=torch.float32, device=device)
@@ -505,7 +619,7 @@ def gpu_arm(args, w, dist, rank, world, device):
         return
     line = {
         "metric": METRIC, "value": round(us_per_row, 4), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": max(3, args.warmup),
+        "steps": args.steps, "warmup": warm_steps,
         "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic",
@@ -514,7 +628,12 @@ def gpu_arm(args, w, dist, rank, world, device):
             "logits": w.dtype, "row_len": "full rows" if full_rows else "ragged (device row_len)",
             "l2": f"inputs larger than L2: {ncopies} rotating copies of {nbytes} B "
                   f"({ncopies * nbytes / 2**20:.0f} MiB > 2x {l2 / 2**20:.0f} MiB L2)",
-            "graph": f"{G} calls per CUDA graph", "parallelism": f"replicas x{world}",
+            "graph": f"{G} calls per CUDA graph; warm-up replays every timed graph first; a "
+                     f"spin kernel ahead of the first event hides the graph's submission",
+            "value_is": "back to back: calls queued one after another on one stream, the next "
+                        "call's blocks resident while this call finishes (programmatic dependent "
+                        "launch); `cold` is one call alone after an L2 flush",
+            "parallelism": f"replicas x{world}",
             "plan": dict(zip(("blocks_per_row", "grid"), tks.plan(w.batch, w.row_stride, w.k,
                                                                   0 if w.dtype == W.F32 else 1))),
         },
@@ -528,6 +647,8 @@ def gpu_arm(args, w, dist, rank, world, device):
                            "what": "torch sum over a 1 GiB fp32 buffer (library kernel, read only)"},
         },
         "cold": cold,
+        "latency": {"back_to_back_us_per_call": round(ms_max * 1e3 / args.steps, 3),
+                    "cold_us_per_call": cold["us_per_call"]},
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_us_row, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(alg_bytes + (0 if full_rows else 4 * w.batch)),
@@ -542,6 +663,8 @@ def gpu_arm(args, w, dist, rank, world, device):
     }
     if sorted_line is not None:
         line["sorted"] = sorted_line
+    if world == 1 and not args.no_configs:
+        line["configs"] = other_configs(tks, torch, args, w.name, stream, device, l2, peak, gpu_id)
     if rank == 0 and world == 1:  # (the CPU baseline is taken at N=1 only)
         line["cpu_baseline"] = cpu_oracle_time(w, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -554,6 +677,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_1m_masked", choices=sorted(W.NAMED) + sorted(W.EXTRA))
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the timing of the other named workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU oracle work for cpu_baseline")
     args = ap.parse_args(argv)
