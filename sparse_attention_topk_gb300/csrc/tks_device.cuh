@@ -56,19 +56,23 @@ constexpr unsigned kStatInternal = 1u << 2;
 struct SlotHdr {
   unsigned epoch;       // calls that used this slot so far
   unsigned used[2];     // digit rounds the last call of each parity used
-  unsigned pad0;
-  // Per parity: barrier arrivals (monotonic within a call) and, next to it so
-  // one 64-bit load reads both, 1 + the highest nonempty first-digit bin of
-  // the row (0 = none yet).
-  struct {
+  // Candidate words [0, cand_dirty) the last call left written: the next call
+  // puts them back to all ones before its first row barrier.
+  unsigned cand_dirty;
+  // Per parity, in one 16-byte word so that one load reads them together:
+  // barrier arrivals (monotonic within a call), 1 + the highest nonempty
+  // first-digit bin of the row (0 = none yet), and the highest of the blocks'
+  // first-round floors (no block's floor lies above the row's threshold bin).
+  struct alignas(16) {
     unsigned arrive;
     unsigned top;
+    unsigned floor;
+    unsigned pad;
   } sync[2];
   // Per parity: OR of the row's first-round keys and OR of their complements
   // (their AND, inverted, so that both start from zero): equal iff every key
   // of the row is the same.
   unsigned keyset[2][2];
-  unsigned pad[4];
 };
 static_assert(sizeof(SlotHdr) == 64, "slot header is one 64-byte line");
 constexpr size_t kSlotHistOff = sizeof(SlotHdr);
@@ -440,6 +444,15 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_acquire_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {

@@ -275,23 +275,24 @@ __device__ __forceinline__ void mbar_wait_bounded(unsigned long long* bar, unsig
 }
 
 // The row barrier after a merge, then the row's counts of bins [lo, top)
-// replace the local ones in h[].  top is the row's maximum (from the word
-// beside the arrival count) when use_top, else nb; it is left in ctl->top.
-// Bounded: on time-out records the error and returns false.
+// replace the local ones in h[].  When use_top (the first round), top is the
+// row's maximum and lo is raised to the row's highest floor (both from the
+// word beside the arrival count), else top is nb; they are left in ctl->lo
+// and ctl->top.  Bounded: on time-out records the error and returns false.
 __device__ __forceinline__ bool merge_wait_load(unsigned* h, int lo, int nb, const unsigned* g,
-                                                unsigned* sync_pair, bool use_top, unsigned target,
+                                                unsigned* sync_word, bool use_top, unsigned target,
                                                 bool skip_arrive, long long limit, Ctl* ctl,
                                                 unsigned* status) {
   constexpr int kPer = kMaxBins / kThreads;
   if (threadIdx.x == 0) {
     // release: this block's adds (all returned before the caller's barrier)
     // are visible to any block that sees the arrival
-    if (!skip_arrive) red_release_add_u32(&sync_pair[0], 1u);
+    if (!skip_arrive) red_release_add_u32(&sync_word[0], 1u);
     unsigned ok = 1u;
-    unsigned long long w = ld_acquire_u64(sync_pair);
-    if ((unsigned)w < target) {
+    uint4 w = ld_acquire_v4(sync_word);
+    if (w.x < target) {
       const unsigned long long t0 = globaltimer_ns();
-      while ((unsigned)(w = ld_acquire_u64(sync_pair)) < target) {
+      while ((w = ld_acquire_v4(sync_word)).x < target) {
         if ((long long)(globaltimer_ns() - t0) > limit) {
           ok = 0u;
           atomicOr(status, kStatTimeout);
@@ -299,12 +300,14 @@ __device__ __forceinline__ bool merge_wait_load(unsigned* h, int lo, int nb, con
         }
       }
     }
-    ctl->top = use_top ? min((unsigned)nb, (unsigned)(w >> 32)) : (unsigned)nb;
+    ctl->top = use_top ? min((unsigned)nb, w.y) : (unsigned)nb;
+    ctl->lo = use_top ? max((unsigned)lo, w.z) : (unsigned)lo;
     ctl->ok = ok;
   }
   __syncthreads();
   if (!ctl->ok) return false;
   const int top = (int)ctl->top;
+  lo = (int)ctl->lo;
   unsigned c[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
@@ -363,38 +366,33 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
                                                     long long limit, Ctl* ctl, unsigned* status,
                                                     int* lo, int* hi, unsigned* gh, bool* cl_pending) {
   constexpr int kPer = kMaxBins / kThreads;
-  static_assert(kPer % 4 == 0, "bins per thread");
+  constexpr int Q = kPer / 4;  // 16-byte vectors of bins per thread
+  static_assert(kPer % 4 == 0 && 8 % Q == 0, "bins per thread");
   const int b0 = (int)threadIdx.x * kPer;
-  unsigned c[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer / 4; ++q) {
-    const uint4 v = reinterpret_cast<const uint4*>(h + b0)[q];
-    c[4 * q] = v.x;
-    c[4 * q + 1] = v.y;
-    c[4 * q + 2] = v.z;
-    c[4 * q + 3] = v.w;
-  }
+  // The sum of my bins, reading my vectors in a rotated order so that the
+  // lanes of a warp spread over all banks.
   unsigned S = 0u;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) S += c[j];
+  for (int q = 0; q < Q; ++q) {
+    const uint4 v = reinterpret_cast<const uint4*>(h + b0)[(q + (int)threadIdx.x / (8 / Q)) % Q];
+    S += (v.x + v.y) + (v.z + v.w);
+  }
   unsigned total;
   const unsigned A = block_suffix_excl(S, &total, ctl);  // this block's elements above my bins
   if (A < k && (threadIdx.x == 0 || A + S >= k)) {
     // the floor is mine: the lowest of my bins with fewer than k above it
     unsigned above = A;
     int f = 0;
-#pragma unroll
     for (int j = kPer - 1; j >= 0; --j) {
       if (above < k) f = j;
-      above += c[j];
+      above += h[b0 + j];
     }
     ctl->lo = (unsigned)(b0 + f);
   }
   if (A == 0u && S != 0u) {  // my bins hold the highest nonempty one
     int tj = 0;
-#pragma unroll
     for (int j = 0; j < kPer; ++j)
-      if (c[j] != 0u) tj = j;
+      if (h[b0 + j] != 0u) tj = j;
     ctl->top = (unsigned)(b0 + tj + 1);
   }
   if (total == 0u && threadIdx.x == 0) ctl->top = 0u;
@@ -405,6 +403,7 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
     *hi = top;
     return true;
   }
+  unsigned c[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
@@ -443,8 +442,11 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
   }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
-  // an atomic with return, so it has been performed by the arrival
-  if (threadIdx.x == 0 && top > 0) ctl->sink = atomicMax(&sync_pair[1], (unsigned)top);
+  // atomics with return, so they have been performed by the arrival
+  if (threadIdx.x == 0) {
+    const unsigned a = top > 0 ? atomicMax(&sync_pair[1], (unsigned)top) : 0u;
+    ctl->sink = a + atomicMax(&sync_pair[2], (unsigned)l);
+  }
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = j * kThreads + threadIdx.x;
@@ -453,6 +455,7 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
   __syncthreads();  // also: every thread has read ctl->top before it is rewritten
   if (!merge_wait_load(h, l, kMaxBins, g, sync_pair, true, target, skip_arrive, limit, ctl, status))
     return false;
+  *lo = (int)ctl->lo;
   *hi = (int)ctl->top;
   return true;
 }
@@ -902,6 +905,45 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
   if (bad) atomicOr(status, kStatInternal);
 }
 
+// Digits of the register finisher are at most kPickBits wide, so that one
+// warp finds the threshold bin among kPickBins counters.
+constexpr int kPickBits = 8;
+constexpr int kPickBins = 1 << kPickBits;
+
+// One warp (all 32 lanes call): the bin of h[0, kPickBins) holding the
+// k_rem-th largest count from the top, with the count above it and its own
+// count, into ctl->pick_* (pick_bin all ones if the counts hold fewer than
+// k_rem).  Lane l owns bins [8l, 8l + 8), read in an order that spreads the
+// lanes over all banks.
+__device__ __forceinline__ void warp_pick(const unsigned* h, unsigned k_rem, Ctl* ctl) {
+  static_assert(kPickBins == 256, "eight bins per lane");
+  const unsigned lane = lane_id();
+  const uint4* h4 = reinterpret_cast<const uint4*>(h) + 2 * lane;
+  const uint4 a = h4[(lane >> 2) & 1u], b = h4[((lane >> 2) + 1u) & 1u];
+  const unsigned S = (a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w);
+  unsigned x = S;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned y = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x += y;
+  }
+  const unsigned A = x - S;  // counts in the lanes above
+  const bool mine = A < k_rem && A + S >= k_rem;
+  if (mine) {
+    unsigned above = A;
+    for (int j = 7; j >= 0; --j) {
+      const unsigned c = h[8 * lane + j];
+      if (above < k_rem && above + c >= k_rem) {
+        ctl->pick_bin = 8 * lane + j;
+        ctl->pick_above = above;
+        ctl->pick_cnt = c;
+      }
+      above += c;
+    }
+  }
+  if (__ballot_sync(0xffffffffu, mine) == 0u && lane == 0) ctl->pick_bin = 0xFFFFFFFFu;
+}
+
 // Candidates a thread keeps in registers in the register finisher.
 constexpr int kRegCand = 8;
 constexpr unsigned kRegCandCap = (unsigned)kRegCand * kThreads;
@@ -964,27 +1006,36 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   const unsigned out_base = k - k_rem;
   uint32_t vk = (or_k ^ and_k) & ~P.kmask;
   uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
+  // two sets of kPickBins counters, used by alternate rounds: a round clears
+  // the set the next one counts into
+  for (int i = threadIdx.x; i < 2 * kPickBins; i += kThreads) h[i] = 0u;
   if (threadIdx.x == 0) ctl->emit_n = 0u;  // read after the rounds' barriers
+  __syncthreads();
   unsigned sel = 0u;
   unsigned live = n;
-  for (;;) {
+  for (int r = 0;; ++r) {
     Digit2 D;
-    if (!next_digit2(vk, vp, digit_width(live), &D)) {
+    if (!next_digit2(vk, vp, min(kPickBits, digit_width(live)), &D)) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
-    const int nb = 1 << (D.kb + D.pb);
-    zero_counters(h, nb);
-    __syncthreads();
+    unsigned* cur = h + (r & 1) * kPickBins;
+    unsigned* nxt = h + ((r + 1) & 1) * kPickBins;
     uint32_t d[kRegCand];
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
       d[j] = digit2_value(D, ck[j], ci[j]);
-      if ((alive >> j) & 1u) atomicAdd(&h[d[j]], 1u);
+      if ((alive >> j) & 1u) atomicAdd(&cur[d[j]], 1u);
     }
+    for (int i = threadIdx.x; i < kPickBins; i += kThreads) nxt[i] = 0u;
     __syncthreads();
-    unsigned bin, above, cnt;
-    if (!pick_bin(h, nb, k_rem, ctl, status, &bin, &above, &cnt)) return;
+    if (threadIdx.x < 32) warp_pick(cur, k_rem, ctl);
+    __syncthreads();
+    const unsigned bin = ctl->pick_bin, above = ctl->pick_above, cnt = ctl->pick_cnt;
+    if (bin == 0xFFFFFFFFu) {
+      if (threadIdx.x == 0) atomicOr(status, kStatInternal);
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
       if (!((alive >> j) & 1u)) continue;
@@ -1061,11 +1112,14 @@ __device__ __forceinline__ Slice slice_geometry(uint32_t L, int part, int group,
 
 // Thread 0: the bulk copies of a resident slice's whole vectors into the
 // on-chip copy, each chunk on its own mbarrier.
+// fence: the buffer may hold generic-proxy writes of this block (an earlier
+// row, a finish) that must be ordered before the copy overwrites it; the
+// first copy of a block's only row needs none.
 template <int DT>
 __device__ __forceinline__ void issue_slice_copy(const Slice& s, const unsigned char* row,
-                                                 unsigned char* sl, Ctl* ctl) {
+                                                 unsigned char* sl, Ctl* ctl, bool fence = true) {
   using E = Elt<DT>;
-  fence_proxy_async_smem();
+  if (fence) fence_proxy_async_smem();
   const unsigned long long pol = policy_evict_first();
   for (int c = 0; c < kChunks; ++c) {
     const int c0 = s.nbv * c / kChunks, c1 = s.nbv * (c + 1) / kChunks;
@@ -1131,6 +1185,39 @@ __device__ __forceinline__ bool row_key_set(const Src& src, unsigned* keyset, un
   return ctl->ok != 0u;
 }
 
+// Candidate words [0, dirty) that the previous call on this slot left
+// written go back to all ones, each block of the row taking a share.  Called
+// before the row's first barrier, which orders these stores before every
+// candidate word of this call is written or polled.
+__device__ __forceinline__ void reset_candidates(uint2* cand, unsigned dirty, int part, int group) {
+  unsigned long long* gc = reinterpret_cast<unsigned long long*>(cand);
+  dirty = min(dirty, (unsigned)kGroupCandCap);
+  const unsigned per = (dirty + (unsigned)group - 1u) / (unsigned)group;
+  const unsigned a = min(dirty, (unsigned)part * per), b = min(dirty, a + per);
+  for (unsigned i = a + threadIdx.x; i < b; i += kThreads) st_relaxed_u64(gc + i, kCandEmpty);
+}
+
+// Clears the other parity's counters of a slot, used by the previous call on
+// it, for the next one; blocks 1..group-1 of the row each take a share.
+__device__ __forceinline__ void clear_other_parity(SlotHdr* slot, unsigned par, unsigned used_other,
+                                                   int part, int group) {
+  const unsigned helpers = (unsigned)group - 1u, me = (unsigned)part - 1u;
+  unsigned* other = reinterpret_cast<unsigned*>(reinterpret_cast<unsigned char*>(slot) + kSlotHistOff) +
+                    (size_t)(par ^ 1u) * kSlotHistWords;
+  const unsigned words = min(used_other, (unsigned)kMaxRounds) * (unsigned)kMaxBins;
+  const unsigned per = ((words / 4 + helpers - 1) / helpers) * 4;
+  const unsigned w0 = min(words, me * per), w1 = min(words, w0 + per);
+  for (unsigned i = w0 / 4 + threadIdx.x; i < w1 / 4; i += kThreads)
+    reinterpret_cast<uint4*>(other)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (me == 0 && threadIdx.x == 0) {
+    slot->sync[par ^ 1u].arrive = 0u;
+    slot->sync[par ^ 1u].top = 0u;
+    slot->sync[par ^ 1u].floor = 0u;
+    slot->keyset[par ^ 1u][0] = 0u;
+    slot->keyset[par ^ 1u][1] = 0u;
+  }
+}
+
 // A row length carried from one row to the next: the clamped length, bit 31
 // set when it had to be clamped; kLenUnknown when not loaded yet.
 constexpr uint32_t kLenUnknown = 0xFFFFFFFFu;
@@ -1166,7 +1253,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   uint4 hdr = make_uint4(0u, 0u, 0u, 0u);
   if (group > 1) {
     slot = reinterpret_cast<SlotHdr*>(p.ws + kWsHeaderBytes + (size_t)(blockIdx.x / group) * kSlotBytes);
-    hdr = ld_relaxed_v4(slot);  // epoch, used[0], used[1]
+    hdr = ld_relaxed_v4(slot);  // epoch, used[0], used[1], cand_dirty
   }
 
   // Valid length (clamped; a bad one is reported); for a block that owns
@@ -1179,6 +1266,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   } else {
     L = row_length(p, r, &bad_len);
   }
+  // This block's slice, with 16-byte aligned interior boundaries; a lone row
+  // of a block whose slice is on chip has its copy issued at once.
+  const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
+  const Slice s = slice_geometry<DT>(L, part, group, row);
+  if (kLean && L > k && threadIdx.x == 0) issue_slice_copy<DT>(s, row, sl, ctl, false);
   const int r_next = r + (int)gridDim.x;
   const bool has_next = group == 1 && r_next < p.batch;
   bool bad_next = false;  // (reported by the next row's own call)
@@ -1210,9 +1302,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   const uint32_t pmax = (1u << pos_bits) - 1u;
   const int nr = num_rounds<DT>(pos_bits);
 
-  // This block's slice, with 16-byte aligned interior boundaries.
-  const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
-  const Slice s = slice_geometry<DT>(L, part, group, row);
   const SliceSrc<DT> src{row, sl, s, p.host_src != 0};
 
   // ---- round 0: one pass over HBM, histogram of the top 12 key bits ----
@@ -1236,7 +1325,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     const int vb0 = s.vb0, nbv = s.nbv;
     // (a block that owns whole rows may have issued this copy already, at the
     // end of its previous row)
-    if (threadIdx.x == 0 && !copy_issued) issue_slice_copy<DT>(s, row, sl, ctl);
+    if (!kLean && threadIdx.x == 0 && !copy_issued) issue_slice_copy<DT>(s, row, sl, ctl);
     copy_issued = false;
     // the unaligned head and tail by plain loads
     const int nh = s.bl - s.lo, nt = s.hi - s.bh;
@@ -1302,6 +1391,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     }
     int lo = 0, hi = nb;
     if (t == 0) {
+      if (group > 1) reset_candidates(slot_cand, hdr.w, part, group);
       const bool skip = p.test_skip_arrive && part == 0;
       if (!round0_bounds_merge(h, offs, k, group > 1, group > 1 ? slot_hist : nullptr,
                                group > 1 ? &slot->sync[par].arrive : nullptr, (unsigned)group, skip,
@@ -1309,7 +1399,12 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
         return false;
       if (gh == nullptr && group > 1) ++nbar;  // the first round's L2 barrier
       // every block of the call has read the epoch: the next call may use the other set
-      if (group > 1 && part == 0 && threadIdx.x == 0) slot->epoch = epoch + 1u;
+      // (and until this call says how many candidate words it wrote, the next
+      // one resets them all)
+      if (group > 1 && part == 0 && threadIdx.x == 0) {
+        slot->epoch = epoch + 1u;
+        slot->cand_dirty = (unsigned)kGroupCandCap;
+      }
       // One first-digit bin holds the whole row: if every key is the same,
       // the answer is the k lowest positions.  Each block ORs and ANDs its
       // keys; a split row exchanges them through the slot (one more row
@@ -1408,11 +1503,17 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   }
 
   // ---- rows split over blocks ----
+  // For the next call on this slot: the digit rounds used (their counters are
+  // cleared by the next call of the other parity) and the candidate words
+  // written (reset by the next call).
+  if (part == 0 && threadIdx.x == 0) {
+    slot->used[par] = (unsigned)(t + 1);
+    slot->cand_dirty = end == kEndCollect ? cnt : 0u;
+  }
   if (part == 0) {
     if (end == kEndCollect && cnt <= kRegCandCap) {
       // Gather the row's candidates straight into registers as they land
-      // (each word starts as all ones), put the words back to all ones for
-      // the next call, then finish in registers.
+      // (each word starts as all ones), then finish in registers.
       unsigned long long* gc = reinterpret_cast<unsigned long long*>(slot_cand);
       unsigned long long e[kRegCand];
 #pragma unroll
@@ -1447,7 +1548,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
         ck[j] = (uint32_t)e[j];
         ci[j] = pmax - (uint32_t)(e[j] >> 32);
         if (i < cnt) {
-          gc[i] = kCandEmpty;
           alive |= 1u << j;
           ok_ |= ck[j]; ak &= ck[j]; oi |= ci[j]; ai &= ci[j];
         }
@@ -1458,7 +1558,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
                           status);
     } else if (end == kEndCollect) {
       // Gather the row's candidates as they land (each slot starts as all
-      // ones), put the slots back to all ones for the next call, then finish.
+      // ones), then finish.
       // The candidates go where this block's slice copy was: every thread must
       // be done reading it (the emission pass) first.
       __syncthreads();
@@ -1497,7 +1597,6 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
           if (i >= cnt) continue;
           const uint2 c2 = make_uint2((uint32_t)e[j], (uint32_t)(e[j] >> 32));
           fc[i] = c2;
-          gc[i] = kCandEmpty;
           const uint32_t inv = pmax - c2.y;
           ok_ |= c2.x; ak &= c2.x; oi |= inv; ai &= inv;
         }
@@ -1506,27 +1605,12 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       if (!ctl->ok) return false;
       finish_on_chip(fc, cnt, k_rem, P, ok_, ak, oi, ai, pmax, h, out_row, k, ctl, status);
     }
-    if (threadIdx.x == 0) slot->used[par] = (unsigned)(t + 1);
   } else {
-    // Clear the other parity's counters, used by the previous call on this
-    // slot, for the next one; the blocks other than the finisher share it.
-    const unsigned helpers = (unsigned)group - 1u, me = (unsigned)part - 1u;
-    unsigned* other = reinterpret_cast<unsigned*>(reinterpret_cast<unsigned char*>(slot) + kSlotHistOff) +
-                      (size_t)(par ^ 1u) * kSlotHistWords;
-    const unsigned words = min(used_other, (unsigned)kMaxRounds) * (unsigned)kMaxBins;
-    const unsigned per = ((words / 4 + helpers - 1) / helpers) * 4;
-    const unsigned w0 = min(words, me * per), w1 = min(words, w0 + per);
-    for (unsigned i = w0 / 4 + threadIdx.x; i < w1 / 4; i += kThreads)
-      reinterpret_cast<uint4*>(other)[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (me == 0 && threadIdx.x == 0) {
-      slot->sync[par ^ 1u].arrive = 0u;
-      slot->sync[par ^ 1u].top = 0u;
-      slot->keyset[par ^ 1u][0] = 0u;
-      slot->keyset[par ^ 1u][1] = 0u;
-    }
+    clear_other_parity(slot, par, used_other, part, group);
   }
   return true;
 }
+
 
 template <int DT, bool kLean>
 __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p) {
