@@ -269,10 +269,15 @@ __device__ __forceinline__ unsigned long long policy_evict_first() {
 
 // ---------------------------------------------------------------------------
 // Block-wide scan (kThreads threads, all must call): sum of v over threads
-// with a higher index.  *total gets the sum over all threads.
+// with a higher index.  *total gets the sum over all threads.  scratch holds
+// kWarps words (ctl->warp32 by default); without the trailing barrier the
+// caller must pass a barrier before scratch is written again.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ unsigned block_suffix_excl(unsigned v, unsigned* total, Ctl* ctl) {
+__device__ __forceinline__ unsigned block_suffix_excl(unsigned v, unsigned* total, Ctl* ctl,
+                                                      unsigned* scratch = nullptr,
+                                                      bool trailing_sync = true) {
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  if (scratch == nullptr) scratch = ctl->warp32;
   unsigned x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -280,17 +285,17 @@ __device__ __forceinline__ unsigned block_suffix_excl(unsigned v, unsigned* tota
     if (lane + off < 32) x += y;
   }
   // x = sum over lanes >= lane of this warp
-  if (lane == 0) ctl->warp32[warp] = x;
+  if (lane == 0) scratch[warp] = x;
   __syncthreads();
   unsigned higher = 0, all = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    const unsigned s = ctl->warp32[w];
+    const unsigned s = scratch[w];
     all += s;
     if (w > (int)warp) higher += s;
   }
   *total = all;
-  __syncthreads();  // warp32 reusable afterwards
+  if (trailing_sync) __syncthreads();  // scratch reusable afterwards
   return (x - v) + higher;
 }
 

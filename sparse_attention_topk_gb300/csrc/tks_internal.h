@@ -22,6 +22,7 @@ struct Params {
   long long spin_limit_ns;
   int32_t cluster;  // 1: each row's `group` blocks form one thread-block cluster
   int32_t host_src; // 1: logits and row lengths are page-locked host memory (plain loads only)
+  int32_t chunk;    // slice length of a row of row_stride elements split over `group` blocks
 };
 
 // The selection kernel's launcher and set-up for each block size (256 and 512

@@ -308,16 +308,21 @@ __device__ __forceinline__ bool merge_wait_load(unsigned* h, int lo, int nb, con
   if (!ctl->ok) return false;
   const int top = (int)ctl->top;
   lo = (int)ctl->lo;
-  unsigned c[kPer];
+  if (top - lo <= kThreads) {
+    const int b = lo + (int)threadIdx.x;
+    if (b < top) h[b] = __ldcg(g + b);
+  } else {
+    unsigned c[kPer];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    c[j] = (b >= lo && b < top) ? __ldcg(g + b) : 0u;
-  }
+    for (int j = 0; j < kPer; ++j) {
+      const int b = j * kThreads + threadIdx.x;
+      c[j] = (b >= lo && b < top) ? __ldcg(g + b) : 0u;
+    }
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    if (b >= lo && b < top) h[b] = c[j];
+    for (int j = 0; j < kPer; ++j) {
+      const int b = j * kThreads + threadIdx.x;
+      if (b >= lo && b < top) h[b] = c[j];
+    }
   }
   __syncthreads();
   return true;
@@ -378,22 +383,33 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
     S += (v.x + v.y) + (v.z + v.w);
   }
   unsigned total;
-  const unsigned A = block_suffix_excl(S, &total, ctl);  // this block's elements above my bins
-  if (A < k && (threadIdx.x == 0 || A + S >= k)) {
-    // the floor is mine: the lowest of my bins with fewer than k above it
+  // (the scan's scratch is ctl->red, not needed again before the next barrier)
+  const unsigned A = block_suffix_excl(S, &total, ctl, ctl->red, false);  // elements above my bins
+  const bool floor_mine = A < k && (threadIdx.x == 0 || A + S >= k);
+  const bool top_mine = A == 0u && S != 0u;  // my bins hold the highest nonempty one
+  if (floor_mine || top_mine) {
+    unsigned c[kPer];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(h + b0)[q];
+      c[4 * q] = v.x;
+      c[4 * q + 1] = v.y;
+      c[4 * q + 2] = v.z;
+      c[4 * q + 3] = v.w;
+    }
+    // the floor: the lowest of my bins with fewer than k above it
     unsigned above = A;
-    int f = 0;
+    int f = 0, tj = 0;
+#pragma unroll
     for (int j = kPer - 1; j >= 0; --j) {
       if (above < k) f = j;
-      above += h[b0 + j];
+      above += c[j];
     }
-    ctl->lo = (unsigned)(b0 + f);
-  }
-  if (A == 0u && S != 0u) {  // my bins hold the highest nonempty one
-    int tj = 0;
+#pragma unroll
     for (int j = 0; j < kPer; ++j)
-      if (h[b0 + j] != 0u) tj = j;
-    ctl->top = (unsigned)(b0 + tj + 1);
+      if (c[j] != 0u) tj = j;
+    if (floor_mine) ctl->lo = (unsigned)(b0 + f);
+    if (top_mine) ctl->top = (unsigned)(b0 + tj + 1);
   }
   if (total == 0u && threadIdx.x == 0) ctl->top = 0u;
   __syncthreads();
@@ -403,13 +419,13 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
     *hi = top;
     return true;
   }
-  unsigned c[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    c[j] = (b >= l && b < top) ? h[b] : 0u;
-  }
   if (gh != nullptr) {
+    unsigned c[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = j * kThreads + threadIdx.x;
+      c[j] = (b >= l && b < top) ? h[b] : 0u;
+    }
     // The row is one thread-block cluster: the adds go to block 0's shared
     // histogram gh (distributed shared memory), each returning this block's
     // offset inside the bin; the cluster barrier replaces the L2 barrier.
@@ -440,17 +456,15 @@ __device__ __forceinline__ bool round0_bounds_merge(unsigned* h, unsigned* offs,
     *hi = rtop;
     return ctl->ok != 0u;
   }
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) c[j] = c[j] ? atomicAdd(&g[j * kThreads + threadIdx.x], c[j]) : 0u;
+  // the bins of the window [l, top), one per thread: add, keep the offset
+  for (int b = l + (int)threadIdx.x; b < top; b += kThreads) {
+    const unsigned cb = h[b];
+    offs[b] = cb ? atomicAdd(&g[b], cb) : 0u;
+  }
   // atomics with return, so they have been performed by the arrival
   if (threadIdx.x == 0) {
     const unsigned a = top > 0 ? atomicMax(&sync_pair[1], (unsigned)top) : 0u;
     ctl->sink = a + atomicMax(&sync_pair[2], (unsigned)l);
-  }
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int b = j * kThreads + threadIdx.x;
-    if (b >= l && b < top) offs[b] = c[j];
   }
   __syncthreads();  // also: every thread has read ctl->top before it is rewritten
   if (!merge_wait_load(h, l, kMaxBins, g, sync_pair, true, target, skip_arrive, limit, ctl, status))
@@ -1088,15 +1102,17 @@ __device__ __forceinline__ uint32_t row_length(const Params& p, int r, bool* bad
 
 // Block `part`'s slice of a row of L elements starting at `row`, with 16-byte
 // aligned interior boundaries.
+// chunk: the slice length for a row of L elements, when the caller knows it
+// (0: computed here).
 template <int DT>
 __device__ __forceinline__ Slice slice_geometry(uint32_t L, int part, int group,
-                                                const unsigned char* row) {
+                                                const unsigned char* row, uint32_t chunk = 0u) {
   using E = Elt<DT>;
   const uint32_t V = E::V;
   const uint32_t mis = (uint32_t)(((uintptr_t)row & 15u) / E::ES);
   auto align_up = [&](uint32_t i) -> uint32_t { return i + ((V - ((mis + i) & (V - 1u))) & (V - 1u)); };
   auto align_down = [&](uint32_t i) -> uint32_t { return i - ((mis + i) & (V - 1u)); };
-  const uint32_t chunk = ((L + (uint32_t)group - 1u) / (uint32_t)group + V - 1u) & ~(V - 1u);
+  if (chunk == 0u) chunk = ((L + (uint32_t)group - 1u) / (uint32_t)group + V - 1u) & ~(V - 1u);
   Slice s;
   s.lo = part == 0 ? 0 : (int)min(L, align_up((uint32_t)part * chunk));
   s.hi = part == group - 1 ? (int)L : (int)min(L, align_up((uint32_t)(part + 1) * chunk));
@@ -1252,7 +1268,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   SlotHdr* slot = nullptr;
   uint4 hdr = make_uint4(0u, 0u, 0u, 0u);
   if (group > 1) {
-    slot = reinterpret_cast<SlotHdr*>(p.ws + kWsHeaderBytes + (size_t)(blockIdx.x / group) * kSlotBytes);
+    slot = reinterpret_cast<SlotHdr*>(p.ws + kWsHeaderBytes + (size_t)r * kSlotBytes);
     hdr = ld_relaxed_v4(slot);  // epoch, used[0], used[1], cand_dirty
   }
 
@@ -1269,7 +1285,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   // This block's slice, with 16-byte aligned interior boundaries; a lone row
   // of a block whose slice is on chip has its copy issued at once.
   const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
-  const Slice s = slice_geometry<DT>(L, part, group, row);
+  const Slice s = slice_geometry<DT>(L, part, group, row, p.row_len ? 0u : (uint32_t)p.chunk);
   if (kLean && L > k && threadIdx.x == 0) issue_slice_copy<DT>(s, row, sl, ctl, false);
   const int r_next = r + (int)gridDim.x;
   const bool has_next = group == 1 && r_next < p.batch;
@@ -1362,7 +1378,7 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     slot_hist = reinterpret_cast<unsigned*>(reinterpret_cast<unsigned char*>(slot) + kSlotHistOff) +
                 (size_t)par * kSlotHistWords;
     slot_cand = reinterpret_cast<uint2*>(p.ws + kWsHeaderBytes + (size_t)p.slots * kSlotBytes +
-                                         (size_t)(blockIdx.x / group) * kCandSlotBytes);
+                                         (size_t)r * kCandSlotBytes);
   }
 
   // ---- digit rounds: merge, threshold, emit; until the threshold bin is
@@ -1635,7 +1651,7 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
     bool copy_issued = false;
     uint32_t len_carry = kLenUnknown;
     if (r < p.batch)
-      select_row<DT, kLean>(p, r, blockIdx.x % p.group, smem, phase_bits, cl_pending, copy_issued,
+      select_row<DT, kLean>(p, r, (int)blockIdx.x - r * p.group, smem, phase_bits, cl_pending, copy_issued,
                             len_carry);
   } else {
     bool copy_issued = false;          // the next row's slice copy is in flight

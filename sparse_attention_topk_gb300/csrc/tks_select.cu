@@ -110,10 +110,11 @@ int device_info(int dev, DeviceInfo* out) {
 }
 
 // Block size: rows split into large slices run with 512 threads (measured:
-// four 1M-element bf16 rows over 37 blocks each 33.0 -> 27.4 us, 64 ragged
-// 64K rows over 2 blocks 17.0 -> 16.2 us); smaller slices and whole rows
-// per block are faster with 256 (fewer warps for the control steps).
-constexpr long long kBigSliceBytes = 48 * 1024;
+// 64 ragged 64K rows over 2 blocks of 128 KiB, 17.6 -> 17.2 us); smaller
+// slices (four 1M-element bf16 rows over 37 blocks of 56 KiB: 14.1 us with
+// 256, 14.7 with 512) and whole rows per block are faster with 256 (fewer
+// warps for the control steps).
+constexpr long long kBigSliceBytes = 96 * 1024;
 std::atomic<long long> g_force_threads{0};
 
 int plan_threads(int32_t batch, int64_t row_stride, int32_t dtype, int group) {
@@ -189,6 +190,13 @@ void plan_launch(const DeviceInfo& d, int32_t batch, int64_t row_stride, int* gr
 }
 
 int workspace_slots(const DeviceInfo& d) { return d.sms * d.blocks_per_sm; }
+
+// The slice length the kernel gives each of `group` blocks of a row of
+// row_stride elements: a ceiling share rounded up to whole 16-byte vectors.
+int32_t slice_chunk(int64_t row_stride, int group, int32_t dtype) {
+  const int64_t v = dtype == TKS_F32 ? 4 : 2;
+  return (int32_t)(((row_stride + group - 1) / group + v - 1) / v * v);
+}
 
 // Whether every block's slice of a row of up to row_stride elements split
 // over `group` blocks fits the on-chip copy (its 16-byte vectors, with one
@@ -328,6 +336,7 @@ static int select_launch(const void* logits, const int32_t* row_len, int32_t bat
   p.spin_limit_ns = g_spin_limit_ns.load();
   p.cluster = cluster ? 1 : 0;
   p.host_src = host_src ? 1 : 0;
+  p.chunk = slice_chunk(row_stride, group, dtype);
   // (the kernel without the streamed, host-memory, cluster and whole-row paths)
   const bool lean = group > 1 && !cluster && !host_src && slices_fit_on_chip(row_stride, group, dtype);
 
@@ -608,6 +617,7 @@ extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_l
   p.spin_limit_ns = g_spin_limit_ns.load();
   p.cluster = 0;
   p.host_src = 0;
+  p.chunk = slice_chunk(row_stride, group, dtype);
   const bool lean = group > 1 && slices_fit_on_chip(row_stride, group, dtype);
 
   cudaLaunchConfig_t cfg;
