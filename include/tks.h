@@ -226,8 +226,18 @@ int tks_plan(int32_t batch, int64_t row_stride, int32_t k, int32_t dtype, int32_
  * call clears the part of the array it uses before its kernel runs, on
  * `stream`.  All calls share the one array, so calls that overlap on the GPU
  * (on different streams, or from several threads) race and give wrong
- * results: serialise them.  Device-side errors of this entry point are not
- * reported by tks_device_status (which covers the allocating entry point).
+ * results: serialise them.
+ *
+ * Device-side errors of this entry point are not reported: tks_device_status
+ * covers only the allocating entry points, and the next call clears the
+ * array's status word.  A row length outside [0, row_stride] is clamped to
+ * that range without notice (the result is that of the clamped length).
+ * After a wait between thread blocks that timed out (a block held back for
+ * longer than TKS_OPT_SPIN_LIMIT_NS) or a failed internal consistency check,
+ * the affected row of out_idx may hold any mix of positions written before
+ * the failure and the values it held before the call; no error code tells
+ * this apart from a good result.  Callers that must detect such failures use
+ * tks_topk_indices and tks_device_status instead.
  */
 #define TKS_NOALLOC_MAX_ROWS 8
 int tks_topk_indices_noalloc(const void *logits, const int32_t *row_len, int32_t batch,

@@ -555,15 +555,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[tks::kNoAllocBy
 extern "C" int tks_topk_indices_noalloc(const void* logits, const int32_t* row_len, int32_t batch,
                                         int64_t row_stride, int32_t k, int32_t dtype,
                                         int32_t* out_idx, void* stream) {
-  if (batch < 0 || row_stride < 0 || row_stride > INT32_MAX || k < 1 || k > TKS_K_MAX)
-    return TKS_E_INVAL;
-  if (dtype != TKS_F32 && dtype != TKS_BF16) return TKS_E_INVAL;
-  if (batch == 0) return TKS_OK;
+  // the same argument checks as tks_topk_indices, then the array's row limit
+  const int arg = check_args(logits, batch, row_stride, k, dtype, out_idx);
+  if (arg != TKS_OK || batch == 0) return arg;
   if (batch > TKS_NOALLOC_MAX_ROWS) return TKS_E_TOO_LARGE;
-  const int es = dtype == TKS_F32 ? 4 : 2;
-  if (out_idx == nullptr || ((uintptr_t)out_idx & 3u) != 0) return TKS_E_INVAL;
-  if (row_stride > 0 && (logits == nullptr || ((uintptr_t)logits % (uintptr_t)es) != 0))
-    return TKS_E_INVAL;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -117,3 +117,14 @@ def test_host_entry_validates_before_any_launch():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         assert tks.topk_indices_host_raw(16, None, 1, 8, 1, 0, 16, 0) == tks.TKS_E_INVAL
+
+
+def test_noalloc_entry_checks_arguments_before_its_row_limit():
+    # argument errors are those of tks_topk_indices, whatever the batch size
+    for args in [(16, None, 9, 8, 1, 0, 0), (16, None, 9, 8, 0, 0, 16), (18, None, 9, 8, 1, 0, 16),
+                 (16, None, 1, 8, 1, 7, 16), (16, None, -1, 8, 1, 0, 16)]:
+        assert tks.topk_indices_noalloc_raw(*args, 0) == tks.TKS_E_INVAL, args
+    # then the array's row limit, still before any CUDA call
+    assert tks.topk_indices_noalloc_raw(16, None, tks.TKS_NOALLOC_MAX_ROWS + 1, 8, 1, 0, 16, 0) == \
+        tks.TKS_E_TOO_LARGE
+    assert tks.topk_indices_noalloc_raw(0, None, 0, 8, 1, 0, 16, 0) == tks.TKS_OK
