@@ -92,7 +92,6 @@ struct Ctl {
   unsigned ok;
   unsigned top;
   unsigned lo;                 // first-round floor bin of this block
-  unsigned emit_n;             // output slots taken by the final emission
   unsigned sink;               // keeps an atomic's returned value live
   unsigned kor, knand;         // OR of the keys and OR of their complements: block's, then row's
   unsigned red[4 * kWarps];

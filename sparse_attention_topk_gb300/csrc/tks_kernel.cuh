@@ -630,10 +630,11 @@ __device__ __forceinline__ void emit_round(const Src& src, const Prefix& P, Digi
 // round an element is written exactly when its key reaches t0), and the
 // write path only for the elements that pass.  The partial edge vectors go
 // through visit_edges.
+// (suf[d - suf_lo]: the row's elements in the bins above bin d)
 template <int DT>
 __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uint32_t t0,
                                                     const Digit& D, unsigned bin, int end,
-                                                    unsigned base, const unsigned* suf,
+                                                    unsigned base, const unsigned* suf, int suf_lo,
                                                     unsigned* offs, int32_t* out_row, unsigned k,
                                                     uint2* cand, bool cand_global, unsigned cap,
                                                     unsigned* status) {
@@ -649,7 +650,7 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
       else
         bad = true;
     } else {
-      const unsigned slot = base + suf[d] + o;
+      const unsigned slot = base + suf[(int)d - suf_lo] + o;
       if (slot < k)
         out_row[slot] = pos;
       else
@@ -924,17 +925,26 @@ __device__ __forceinline__ void finish_on_chip(const uint2* cand, unsigned n, un
 constexpr int kPickBits = 8;
 constexpr int kPickBins = 1 << kPickBits;
 
-// One warp (all 32 lanes call): the bin of h[0, kPickBins) holding the
-// k_rem-th largest count from the top, with the count above it and its own
-// count, into ctl->pick_* (pick_bin all ones if the counts hold fewer than
-// k_rem).  Lane l owns bins [8l, 8l + 8), read in an order that spreads the
-// lanes over all banks.
-__device__ __forceinline__ void warp_pick(const unsigned* h, unsigned k_rem, Ctl* ctl) {
+// The threshold bin of a digit round: the bin holding the k_rem-th largest
+// element, the count above it and its own count (bin all ones when the counts
+// hold fewer than k_rem elements).
+struct Pick {
+  unsigned bin, above, cnt;
+};
+
+// Every lane of the calling warp gets the pick over the counts h[0,
+// kPickBins).  Lane l owns bins [8l, 8l + 8), read in an order that spreads
+// the lanes over all banks; a suffix scan over the lanes finds the lane that
+// holds the threshold, which broadcasts its bin.
+__device__ __forceinline__ Pick warp_pick(const unsigned* h, unsigned k_rem) {
   static_assert(kPickBins == 256, "eight bins per lane");
   const unsigned lane = lane_id();
   const uint4* h4 = reinterpret_cast<const uint4*>(h) + 2 * lane;
-  const uint4 a = h4[(lane >> 2) & 1u], b = h4[((lane >> 2) + 1u) & 1u];
-  const unsigned S = (a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w);
+  const bool rot = ((lane >> 2) & 1u) != 0u;
+  const uint4 a = h4[rot ? 1 : 0], b = h4[rot ? 0 : 1];
+  const uint4 lo4 = rot ? b : a, hi4 = rot ? a : b;
+  const unsigned c[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+  const unsigned S = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
   unsigned x = S;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -943,19 +953,46 @@ __device__ __forceinline__ void warp_pick(const unsigned* h, unsigned k_rem, Ctl
   }
   const unsigned A = x - S;  // counts in the lanes above
   const bool mine = A < k_rem && A + S >= k_rem;
-  if (mine) {
-    unsigned above = A;
-    for (int j = 7; j >= 0; --j) {
-      const unsigned c = h[8 * lane + j];
-      if (above < k_rem && above + c >= k_rem) {
-        ctl->pick_bin = 8 * lane + j;
-        ctl->pick_above = above;
-        ctl->pick_cnt = c;
-      }
-      above += c;
+  unsigned bin = 0u, above = 0u, cnt = 0u, acc = A;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (acc < k_rem && acc + c[j] >= k_rem) {
+      bin = 8u * lane + (unsigned)j;
+      above = acc;
+      cnt = c[j];
     }
+    acc += c[j];
   }
-  if (__ballot_sync(0xffffffffu, mine) == 0u && lane == 0) ctl->pick_bin = 0xFFFFFFFFu;
+  const unsigned m = __ballot_sync(0xffffffffu, mine);
+  if (m == 0u) return {0xFFFFFFFFu, 0u, 0u};
+  const int src = __ffs((int)m) - 1;
+  return {__shfl_sync(0xffffffffu, bin, src), __shfl_sync(0xffffffffu, above, src),
+          __shfl_sync(0xffffffffu, cnt, src)};
+}
+
+// Every lane of the calling warp gets the pick over the counts h[lo, hi) (at
+// most 32 bins, one per lane) for k_rem, and the warp writes the exclusive
+// suffix sums of those bins (the elements in the bins above each) to
+// sw[b - lo].  No branch around the warp-wide steps.
+__device__ __forceinline__ Pick warp_window_pick(const unsigned* h, int lo, int hi, unsigned k_rem,
+                                                 unsigned* sw) {
+  const unsigned lane = lane_id();
+  const int b = lo + (int)lane;
+  const bool in = b < hi;
+  const unsigned c = in ? h[b] : 0u;
+  unsigned x = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned y = __shfl_down_sync(0xffffffffu, x, off);
+    x += lane + off < 32 ? y : 0u;
+  }
+  const unsigned a = x - c;  // the elements in the bins above mine
+  if (in) sw[lane] = a;
+  const bool found = in && a < k_rem && a + c >= k_rem;
+  const unsigned m = __ballot_sync(0xffffffffu, found);
+  if (m == 0u) return {0xFFFFFFFFu, 0u, 0u};
+  const int src = __ffs((int)m) - 1;
+  return {(unsigned)(lo + src), __shfl_sync(0xffffffffu, a, src), __shfl_sync(0xffffffffu, c, src)};
 }
 
 // Candidates a thread keeps in registers in the register finisher.
@@ -1020,10 +1057,10 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   const unsigned out_base = k - k_rem;
   uint32_t vk = (or_k ^ and_k) & ~P.kmask;
   uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
-  // two sets of kPickBins counters, used by alternate rounds: a round clears
-  // the set the next one counts into
-  for (int i = threadIdx.x; i < 2 * kPickBins; i += kThreads) h[i] = 0u;
-  if (threadIdx.x == 0) ctl->emit_n = 0u;  // read after the rounds' barriers
+  // three sets of kPickBins counters, used by the rounds in turn: a round
+  // clears the set the next one counts into, and every warp finds the
+  // threshold bin itself, so that a round needs one barrier
+  for (int i = threadIdx.x; i < 3 * kPickBins; i += kThreads) h[i] = 0u;
   __syncthreads();
   unsigned sel = 0u;
   unsigned live = n;
@@ -1033,8 +1070,8 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
-    unsigned* cur = h + (r & 1) * kPickBins;
-    unsigned* nxt = h + ((r + 1) & 1) * kPickBins;
+    unsigned* cur = h + (r % 3) * kPickBins;
+    unsigned* nxt = h + ((r + 1) % 3) * kPickBins;
     uint32_t d[kRegCand];
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
@@ -1043,29 +1080,28 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
     }
     for (int i = threadIdx.x; i < kPickBins; i += kThreads) nxt[i] = 0u;
     __syncthreads();
-    if (threadIdx.x < 32) warp_pick(cur, k_rem, ctl);
-    __syncthreads();
-    const unsigned bin = ctl->pick_bin, above = ctl->pick_above, cnt = ctl->pick_cnt;
-    if (bin == 0xFFFFFFFFu) {
+    const Pick pk = warp_pick(cur, k_rem);
+    if (pk.bin == 0xFFFFFFFFu) {
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
       if (!((alive >> j) & 1u)) continue;
-      if (d[j] > bin) sel |= 1u << j;
-      if (d[j] != bin) alive &= ~(1u << j);
+      if (d[j] > pk.bin) sel |= 1u << j;
+      if (d[j] != pk.bin) alive &= ~(1u << j);
     }
-    k_rem -= above;
-    if (cnt == k_rem) {
+    k_rem -= pk.above;
+    if (pk.cnt == k_rem) {
       sel |= alive;
       break;
     }
-    live = cnt;
+    live = pk.cnt;
   }
-  // Distinct slots from out_base on: each warp takes a run of them with one
-  // shared add, its lanes place their candidates by ballot ranks.
-  const unsigned lane = lane_id(), lt = (1u << lane) - 1u;
+  // Distinct slots from out_base on: each warp takes a run of them after the
+  // runs of the warps before it, its lanes place their candidates by ballot
+  // ranks.
+  const unsigned lane = lane_id(), lt = (1u << lane) - 1u, warp = threadIdx.x >> 5;
   unsigned m[kRegCand];
   unsigned wtotal = 0u;
 #pragma unroll
@@ -1073,9 +1109,11 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
     m[j] = __ballot_sync(0xffffffffu, (sel >> j) & 1u);
     wtotal += (unsigned)__popc(m[j]);
   }
-  unsigned wbase = 0u;
-  if (lane == 0 && wtotal) wbase = atomicAdd(&ctl->emit_n, wtotal);
-  unsigned slot = out_base + __shfl_sync(0xffffffffu, wbase, 0);
+  if (lane == 0) ctl->warp32[warp] = wtotal;
+  __syncthreads();
+  unsigned slot = out_base;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) slot += w < (int)warp ? ctl->warp32[w] : 0u;
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kRegCand; ++j) {
@@ -1446,7 +1484,26 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     }
     if (group == 1) zero_counters(offs, nb);
     unsigned bin, above;
-    if (!pick_bin_range(h, lo, hi, nb, k_rem, ctl, status, &bin, &above, &cnt)) return false;
+    const unsigned* suf = h;  // the row's elements above each bin of this round
+    int suf_lo = 0;
+    if (kLean && t == 0 && hi - lo <= 32) {
+      // every warp finds the threshold bin and keeps its own suffix sums (in
+      // the unused local candidate area): no block-wide step
+      unsigned* sw = reinterpret_cast<unsigned*>(lcand) + (threadIdx.x >> 5) * 32u;
+      const Pick pk = warp_window_pick(h, lo, hi, k_rem, sw);
+      __syncwarp();
+      if (pk.bin == 0xFFFFFFFFu) {
+        if (threadIdx.x == 0) atomicOr(status, kStatInternal);
+        return false;
+      }
+      bin = pk.bin;
+      above = pk.above;
+      cnt = pk.cnt;
+      suf = sw;
+      suf_lo = lo;
+    } else if (!pick_bin_range(h, lo, hi, nb, k_rem, ctl, status, &bin, &above, &cnt)) {
+      return false;
+    }
     const unsigned need = k_rem - above;
     end = cnt == need ? kEndFinal : cnt <= cap ? kEndCollect : kEndAbove;
     // (a round that only passes the threshold on, with nothing above its bin
@@ -1454,9 +1511,14 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     if (end != kEndAbove || above != 0u) {
       const uint32_t t0 = (end == kEndAbove ? bin + 1u : bin) << D.shift;
       if (t == 0 && (kLean || s.resident) && !(end == kEndAbove && t0 == 0u))
-        emit_first_resident(src, t0, D, bin, end, base, h, offs, out_row, k, cand, group > 1, cap,
-                            status);
-      else if (kLean || s.resident)
+        emit_first_resident(src, t0, D, bin, end, base, suf, suf_lo, offs, out_row, k, cand,
+                            group > 1, cap, status);
+      else if (suf != h) {
+        // (the warp-kept suffix sums serve the first-round pass above only,
+        // which a first round that has anything to emit always takes)
+        if (threadIdx.x == 0) atomicOr(status, kStatInternal);
+        return false;
+      } else if (kLean || s.resident)
         later_pass_resident<DT, true>(src, P, D, pmax, nullptr, bin, end, base, h, offs, out_row, k,
                                       cand, group > 1, cap, status);
       else
