@@ -34,6 +34,12 @@ struct Elt<0> {  // fp32
   __device__ static __forceinline__ void store(unsigned char* dst, uint32_t raw) {
     *reinterpret_cast<uint32_t*>(dst) = raw;
   }
+  // For a threshold key t0 of a value >= +0.0 (top key bit set): key(raw) >=
+  // t0 exactly when the raw bits, read as a signed integer, are >= sthr(t0)
+  // (negative values have the sign bit set and lie below every such value).
+  __device__ static __forceinline__ int sraw(const uint4& x, int j) { return (int)lane(x, j); }
+  __device__ static __forceinline__ int sthr(uint32_t t0) { return (int)(t0 ^ 0x80000000u); }
+  static constexpr uint32_t kKeyTop = 0x80000000u;
 };
 template <>
 struct Elt<1> {  // bf16
@@ -51,6 +57,13 @@ struct Elt<1> {  // bf16
   __device__ static __forceinline__ void store(unsigned char* dst, uint32_t raw) {
     *reinterpret_cast<uint16_t*>(dst) = (uint16_t)raw;
   }
+  // (as for fp32, on the 16-bit patterns)
+  __device__ static __forceinline__ int sraw(const uint4& x, int j) {
+    const uint32_t w = (j >> 1) == 0 ? x.x : (j >> 1) == 1 ? x.y : (j >> 1) == 2 ? x.z : x.w;
+    return (j & 1) ? (int)w >> 16 : (int)(w << 16) >> 16;
+  }
+  __device__ static __forceinline__ int sthr(uint32_t t0) { return (int)(int16_t)(uint16_t)(t0 ^ 0x8000u); }
+  static constexpr uint32_t kKeyTop = 0x8000u;
 };
 
 // One block's share of a row.
@@ -664,6 +677,7 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
   const Slice& s = src.s;
   const uint4* sv = reinterpret_cast<const uint4*>(src.sm);
   const int va = s.vb0, vb = s.vb0 + s.nbv;
+  const int st0 = E::sthr(t0);
   for (int v0 = va + (int)threadIdx.x; v0 < vb; v0 += B * kThreads) {
     uint4 x[B];
 #pragma unroll
@@ -673,12 +687,21 @@ __device__ __forceinline__ void emit_first_resident(const SliceSrc<DT>& src, uin
     }
     // which of the B * U elements are written (a compact unrolled test) ...
     unsigned sel = 0u;
+    if (t0 >= E::kKeyTop) {
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int v = v0 + b * kThreads;
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
 #pragma unroll
-      for (int j = 0; j < U; ++j)
-        sel |= (v < vb && E::key(E::lane(x[b], j)) >= t0 ? 1u : 0u) << (b * U + j);
+        for (int j = 0; j < U; ++j) sel |= (v < vb && E::sraw(x[b], j) >= st0 ? 1u : 0u) << (b * U + j);
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int v = v0 + b * kThreads;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+          sel |= (v < vb && E::key(E::lane(x[b], j)) >= t0 ? 1u : 0u) << (b * U + j);
+      }
     }
     // ... then one copy of the write path for those (rare) elements, keys
     // re-read from shared memory, so the loop stays small; two at a time, so
@@ -1320,11 +1343,10 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   } else {
     L = row_length(p, r, &bad_len);
   }
-  // This block's slice, with 16-byte aligned interior boundaries; a lone row
-  // of a block whose slice is on chip has its copy issued at once.
+  // This block's slice, with 16-byte aligned interior boundaries (the lean
+  // kernel has issued its copy on entry).
   const unsigned char* row = p.logits + (int64_t)r * p.row_stride * E::ES;
   const Slice s = slice_geometry<DT>(L, part, group, row, p.row_len ? 0u : (uint32_t)p.chunk);
-  if (kLean && L > k && threadIdx.x == 0) issue_slice_copy<DT>(s, row, sl, ctl, false);
   const int r_next = r + (int)gridDim.x;
   const bool has_next = group == 1 && r_next < p.batch;
   bool bad_next = false;  // (reported by the next row's own call)
@@ -1705,6 +1727,17 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   // (its writes to the inputs, the outputs and the workspace included) is
   // complete after it.
   grid_dependency_wait();
+  if (kLean && threadIdx.x == 0) {
+    // the one row's slice copy goes out before anything else
+    const int r = blockIdx.x / p.group, part = (int)blockIdx.x - r * p.group;
+    bool bad;
+    const uint32_t L = r < p.batch ? row_length(p, r, &bad) : 0u;
+    if (L > (uint32_t)p.k) {
+      const unsigned char* row = p.logits + (int64_t)r * p.row_stride * Elt<DT>::ES;
+      const Slice s = slice_geometry<DT>(L, part, p.group, row, p.row_len ? 0u : (uint32_t)p.chunk);
+      issue_slice_copy<DT>(s, row, smem + kSliceOff, ctl, false);
+    }
+  }
   __syncthreads();
   unsigned phase_bits = 0u;
   bool cl_pending = false;  // arrived at the cluster barrier that ends block 0's reads
