@@ -478,6 +478,10 @@ def gpu_arm(args, w, dist, rank, world, device):
     import sparse_attention_topk_gb300 as tks
 
     tks.load()
+    if args.hist_variant == "aggregated":
+        # the measurement build: warp-aggregated first-round adds
+        from sparse_attention_topk_gb300 import _build
+        tks.use(_build.build(hist_aggregate=True))
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
     props = torch.cuda.get_device_properties(device)
@@ -643,6 +647,8 @@ def gpu_arm(args, w, dist, rank, world, device):
                         "call's blocks resident while this call finishes (programmatic dependent "
                         "launch); `cold` is one call alone after an L2 flush",
             "parallelism": f"replicas x{world}",
+            "first_round_histogram": "plain shared-memory adds" if args.hist_variant == "plain"
+                                     else "warp-aggregated adds (measurement build)",
             "plan": dict(zip(("blocks_per_row", "grid"), tks.plan(w.batch, w.row_stride, w.k,
                                                                   0 if w.dtype == W.F32 else 1))),
         },
@@ -686,6 +692,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_1m_masked", choices=sorted(W.NAMED) + sorted(W.EXTRA))
+    ap.add_argument("--hist-variant", choices=["plain", "aggregated"], default="plain",
+                    help="aggregated: the measurement build whose first-round histogram "
+                         "uses warp-aggregated (match_any) adds")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the timing of the other named workloads")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

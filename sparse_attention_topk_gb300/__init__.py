@@ -93,6 +93,16 @@ def load(path: str | None = None):
         return lib
 
 
+def use(path: str):
+    """Make the library at `path` (a build of libtks.so, e.g. the measurement
+    build with warp-aggregated first-round adds) the one every call uses."""
+    global _lib
+    lib = load(path)
+    with _lock:
+        _lib = lib
+    return lib
+
+
 def status_string(status: int) -> str:
     return load().tks_status_string(int(status)).decode()
 
@@ -252,7 +262,7 @@ def topk_indices(logits, k: int, row_len=None, out=None, stream=None, sorted: bo
 
 
 __all__ = [
-    "topk_indices", "topk_indices_raw", "topk_indices_host_raw", "topk_indices_noalloc_raw", "topk_indices_sorted_raw", "device_status", "set_option", "plan", "release",
+    "use", "topk_indices", "topk_indices_raw", "topk_indices_host_raw", "topk_indices_noalloc_raw", "topk_indices_sorted_raw", "device_status", "set_option", "plan", "release",
     "status_string", "version", "load", "lib_path", "build", "TksError", "SIGNATURES",
     "TKS_F32", "TKS_BF16", "TKS_OK", "TKS_E_INVAL", "TKS_E_UNSUPPORTED", "TKS_E_CUDA",
     "TKS_E_TIMEOUT", "TKS_E_INTERNAL", "TKS_E_ROW_LEN", "TKS_E_TOO_LARGE", "TKS_NOALLOC_MAX_ROWS",

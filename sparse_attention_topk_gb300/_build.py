@@ -39,9 +39,18 @@ def up_to_date(path: str = LIB_PATH) -> bool:
     return all(os.path.getmtime(s) <= t for s in DEPENDS)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, out: str = LIB_PATH) -> str:
-    """Compile libtks.so unless it is newer than every source; returns its path."""
-    if not force and out == LIB_PATH and up_to_date(out):
+# A measurement build: the first-round histogram with warp-aggregated adds
+# (match_any) instead of plain shared-memory adds, otherwise the same library.
+HIST_AGGREGATE_PATH = os.path.join(BUILD_DIR, "libtks_hist_aggregate.so")
+
+
+def build(force: bool = False, verbose_ptxas: bool = False, out: str = LIB_PATH,
+          hist_aggregate: bool = False) -> str:
+    """Compile libtks.so unless it is newer than every source; returns its path.
+    hist_aggregate: the measurement build (HIST_AGGREGATE_PATH by default)."""
+    if hist_aggregate and out == LIB_PATH:
+        out = HIST_AGGREGATE_PATH
+    if not force and up_to_date(out):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tag = f".tmp{os.getpid()}"
@@ -51,6 +60,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, out: str = LIB_PATH)
     procs = []
     for src, obj in zip(SOURCES, objs):
         cmd = [nvcc, *NVCC_FLAGS, f"-I{INCLUDE}", f"-I{CSRC}", "-c", src, "-o", obj]
+        if hist_aggregate:
+            cmd.insert(1, "-DTKS_HIST_AGGREGATE=1")
         if verbose_ptxas:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd)))

@@ -13,6 +13,12 @@
 #include "tks_device.cuh"
 #include "tks_internal.h"
 
+// 1: the first-round histogram of resident slices uses warp-aggregated adds
+// (a measurement build; the library proper uses plain shared-memory adds).
+#ifndef TKS_HIST_AGGREGATE
+#define TKS_HIST_AGGREGATE 0
+#endif
+
 namespace tks {
 namespace TKS_VARIANT {
 
@@ -122,6 +128,26 @@ struct SliceSrc {
       for (int b = 0; b < B; ++b) {
         const int v = v0 + b * kThreads;
         if (v < vb) vec(x[b], s.o + v * U, (1u << U) - 1u, f);
+      }
+    }
+  }
+
+  // The first-round histogram with warp-aggregated adds (the build with
+  // TKS_HIST_AGGREGATE=1, kept to measure that choice against the plain adds
+  // of visit_range): the lanes of a warp that hold the same bin (match_any)
+  // add their count with one atomic.  Every lane runs the same number of
+  // steps, as match_any needs all 32.
+  __device__ __forceinline__ void hist_aggregated(int va, int vb, unsigned* h) const {
+    using E = Elt<DT>;
+    const uint4* sv = reinterpret_cast<const uint4*>(sm);
+    for (int v0 = va; v0 < vb; v0 += kThreads) {
+      const int v = v0 + (int)threadIdx.x;
+      const uint4 x = v < vb ? sv[v] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t bin = E::key(E::lane(x, j)) >> E::kShift0;
+        const unsigned m = __match_any_sync(0xffffffffu, v < vb ? bin : 0xFFFFFFFFu);
+        if (v < vb && __ffs((int)m) - 1 == (int)lane_id()) atomicAdd(&h[bin], (unsigned)__popc(m));
       }
     }
   }
@@ -1417,7 +1443,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       if (c1 > c0) {
         mbar_wait_bounded(&ctl->mbar[c], (phase_bits >> c) & 1u, p.spin_limit_ns, ctl, status);
         phase_bits ^= 1u << c;
+#if TKS_HIST_AGGREGATE
+        src.hist_aggregated(vb0 + c0, vb0 + c1, h);
+#else
         src.visit_range(vb0 + c0, vb0 + c1, f0);
+#endif
       }
     }
   } else {
