@@ -168,21 +168,21 @@ int tks_release(void);
  *                            before giving up with TKS_E_TIMEOUT (default 1 s)
  *   TKS_OPT_MIN_PER_BLOCK    automatic split: rows of at most 4096 elements
  *                            stay on one block; longer rows get one block per
- *                            this many elements (default 2048, chosen by
+ *                            this many elements (default 4096, chosen by
  *                            measurement), leaving one block slot of the
  *                            device free when the row count allows
  *   TKS_OPT_TEST_SKIP_ARRIVE test only: 1 makes the first block of each row
  *                            skip its first arrival, so the others' waits run
  *                            out and report TKS_E_TIMEOUT; 0 = off
  *   TKS_OPT_FORCE_THREADS    threads per block: 0 = automatic (512 for rows
- *                            split into slices of 48 KiB or more, else 256),
+ *                            split into slices of 96 KiB or more, else 256),
  *                            or 256 or 512
  *   TKS_OPT_CLUSTER          rows split over one thread-block cluster, whose
  *                            blocks merge through distributed shared memory:
- *                            0 = automatic (rows of up to 1 MiB, about 32 KiB
- *                            per block), 1 = never, n >= 2 = clusters of n
- *                            blocks (at most what the device schedules) for
- *                            every row they fit
+ *                            0 = automatic and 1 = never (split rows merge
+ *                            through L2, measured faster), n >= 2 = clusters
+ *                            of n blocks (at most what the device schedules)
+ *                            for every row they fit
  * Returns TKS_E_INVAL for an unknown option, a negative value or (for
  * TKS_OPT_FORCE_THREADS) a block size other than 0, 256 or 512.
  */

@@ -76,7 +76,7 @@ std::map<std::pair<int, void*>, Workspace> g_ws;
 
 std::atomic<long long> g_force_group{0};
 std::atomic<long long> g_spin_limit_ns{1000000000LL};
-std::atomic<long long> g_min_per_block{2048};
+std::atomic<long long> g_min_per_block{4096};
 constexpr long long kLoneRowMax = 4096;  // rows this short are never split
 std::atomic<long long> g_test_skip_arrive{0};
 
@@ -125,27 +125,21 @@ int plan_threads(int32_t batch, int64_t row_stride, int32_t dtype, int group) {
   return group > 1 && (row_stride + group - 1) / group * es >= kBigSliceBytes ? 512 : 256;
 }
 
-// Rows up to kClusterRowBytes are split over one thread-block cluster (its
-// blocks merge through distributed shared memory and the cluster barrier)
-// with about kClusterSliceBytes per block; longer rows over more blocks
-// through L2.  TKS_OPT_CLUSTER: 0 automatic, 1 never, n >= 2 clusters of n.
-constexpr long long kClusterSliceBytes = 32 * 1024;
+// Rows split over one thread-block cluster (its blocks merge through
+// distributed shared memory and the cluster barrier) only when asked for:
+// TKS_OPT_CLUSTER n >= 2 gives clusters of n blocks.  Automatically (0) and
+// with 1, split rows merge through L2: measured back to back, fp32 rows of
+// 32K to 512K elements took 9.1-10.0 us split through L2 at about 4096
+// elements per block and 9.8-12.0 us in the clusters chosen before (up to 16
+// blocks of about 32 KiB).
 std::atomic<long long> g_cluster_opt{0};
 
 int plan_cluster(const DeviceInfo& d, int32_t batch, int64_t row_stride, int32_t dtype) {
   const long long opt = g_cluster_opt.load();
-  if (opt == 1 || g_force_group.load() > 0 || d.max_cluster < 2) return 0;
-  const long long es = dtype == TKS_F32 ? 4 : 2, bytes = row_stride * es;
+  if (opt < 2 || g_force_group.load() > 0 || d.max_cluster < 2) return 0;
+  const long long es = dtype == TKS_F32 ? 4 : 2;
   if (row_stride <= kLoneRowMax) return 0;
-  int n;
-  if (opt >= 2) {
-    n = (int)(opt < d.max_cluster ? opt : d.max_cluster);
-  } else {
-    if (bytes > (long long)d.max_cluster * kClusterSliceBytes * 2) return 0;
-    long long want = (bytes + kClusterSliceBytes - 1) / kClusterSliceBytes;
-    if (want < 2) want = 2;
-    n = (int)(want < d.max_cluster ? want : d.max_cluster);
-  }
+  const int n = (int)(opt < d.max_cluster ? opt : d.max_cluster);
   const int cap = d.sms * d.blocks_per_sm;
   if ((long long)batch * n > cap - 1) return 0;
   if ((row_stride + n - 1) / n * es > kSliceBytes) return 0;  // slices stay on chip
@@ -502,7 +496,7 @@ extern "C" int tks_set_option(int option, int64_t value) {
   switch (option) {
     case TKS_OPT_FORCE_GROUP: g_force_group.store(value); return TKS_OK;
     case TKS_OPT_SPIN_LIMIT_NS: g_spin_limit_ns.store(value > 0 ? value : 1); return TKS_OK;
-    case TKS_OPT_MIN_PER_BLOCK: g_min_per_block.store(value > 0 ? value : 2048); return TKS_OK;
+    case TKS_OPT_MIN_PER_BLOCK: g_min_per_block.store(value > 0 ? value : 4096); return TKS_OK;
     case TKS_OPT_TEST_SKIP_ARRIVE: g_test_skip_arrive.store(value ? 1 : 0); return TKS_OK;
     case TKS_OPT_CLUSTER: g_cluster_opt.store(value); return TKS_OK;
     case TKS_OPT_FORCE_THREADS:
