@@ -306,7 +306,7 @@ class DeviceTiming:
     submits the graphs, so the timed region holds the K calls and nothing else.
     """
 
-    SPIN_CYCLES = 200_000  # ~0.1 ms at the GB300's clocks
+    SPIN_CYCLES = 2_000_000  # ~1 ms at the GB300's clocks: longer than the host needs to submit
 
     def __init__(self, tks, torch, w, stream, device, l2):
         self.tks, self.torch, self.w, self.stream, self.device, self.l2 = tks, torch, w, stream, device, l2
