@@ -465,6 +465,22 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {
   return v;
 }
 
+// Predicated forms (no branch around the access): a shared-memory add and a
+// global store that happen only when p holds.
+__device__ __forceinline__ void red_shared_add_if(bool p, unsigned* addr, unsigned v) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q red.shared.add.u32 [%1], %2;\n\t}" ::"r"(
+          (unsigned)p),
+      "r"(smem_u32(addr)), "r"(v)
+      : "memory");
+}
+__device__ __forceinline__ void st_global_s32_if(bool p, int32_t* addr, int32_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.global.s32 [%1], %2;\n\t}" ::"r"(
+                   (unsigned)p),
+               "l"(addr), "r"(v)
+               : "memory");
+}
+
 // Candidate words in global memory, written and polled without caching.
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -1102,15 +1102,18 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
                                                     uint32_t and_k, uint32_t or_i, uint32_t and_i,
                                                     unsigned n, uint32_t pmax, unsigned* h,
                                                     int32_t* out_row, unsigned k, Ctl* ctl,
-                                                    unsigned* status) {
+                                                    unsigned* status, bool counters_clear = false) {
   const unsigned out_base = k - k_rem;
   uint32_t vk = (or_k ^ and_k) & ~P.kmask;
   uint32_t vp = (or_i ^ and_i) & pmax & ~P.pmask;
   // three sets of kPickBins counters, used by the rounds in turn: a round
   // clears the set the next one counts into, and every warp finds the
-  // threshold bin itself, so that a round needs one barrier
-  for (int i = threadIdx.x; i < 3 * kPickBins; i += kThreads) h[i] = 0u;
-  __syncthreads();
+  // threshold bin itself, so that a round needs one barrier (the caller may
+  // have cleared them already, off the critical path)
+  if (!counters_clear) {
+    for (int i = threadIdx.x; i < 3 * kPickBins; i += kThreads) h[i] = 0u;
+    __syncthreads();
+  }
   unsigned sel = 0u;
   unsigned live = n;
   for (int r = 0;; ++r) {
@@ -1125,7 +1128,7 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
       d[j] = digit2_value(D, ck[j], ci[j]);
-      if ((alive >> j) & 1u) atomicAdd(&cur[d[j]], 1u);
+      red_shared_add_if((alive >> j) & 1u, &cur[d[j]], 1u);
     }
     for (int i = threadIdx.x; i < kPickBins; i += kThreads) nxt[i] = 0u;
     __syncthreads();
@@ -1134,12 +1137,16 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
       if (threadIdx.x == 0) atomicOr(status, kStatInternal);
       return;
     }
+    // (branch-free: a live candidate above the bin is selected, one in it
+    // stays live, the rest drop out)
+    unsigned up = 0u, in = 0u;
 #pragma unroll
     for (int j = 0; j < kRegCand; ++j) {
-      if (!((alive >> j) & 1u)) continue;
-      if (d[j] > pk.bin) sel |= 1u << j;
-      if (d[j] != pk.bin) alive &= ~(1u << j);
+      up |= (d[j] > pk.bin ? 1u : 0u) << j;
+      in |= (d[j] == pk.bin ? 1u : 0u) << j;
     }
+    sel |= alive & up;
+    alive &= in;
     k_rem -= pk.above;
     if (pk.cnt == k_rem) {
       sel |= alive;
@@ -1149,7 +1156,7 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   }
   // Distinct slots from out_base on: each warp takes a run of them after the
   // runs of the warps before it, its lanes place their candidates by ballot
-  // ranks.
+  // ranks (predicated stores, no branch per candidate).
   const unsigned lane = lane_id(), lt = (1u << lane) - 1u, warp = threadIdx.x >> 5;
   unsigned m[kRegCand];
   unsigned wtotal = 0u;
@@ -1166,13 +1173,10 @@ __device__ __forceinline__ void finish_in_registers(const uint32_t (&ck)[kRegCan
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kRegCand; ++j) {
-    if ((sel >> j) & 1u) {
-      const unsigned sj = slot + (unsigned)__popc(m[j] & lt);
-      if (sj < k)
-        out_row[sj] = (int)(pmax - ci[j]);
-      else
-        bad = true;
-    }
+    const bool s_j = ((sel >> j) & 1u) != 0u;
+    const unsigned sj = slot + (unsigned)__popc(m[j] & lt);
+    st_global_s32_if(s_j && sj < k, out_row + sj, (int32_t)(pmax - ci[j]));
+    bad |= s_j && sj >= k;
     slot += (unsigned)__popc(m[j]);
   }
   if (bad) atomicOr(status, kStatInternal);
@@ -1643,7 +1647,11 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
   if (part == 0) {
     if (end == kEndCollect && cnt <= kRegCandCap) {
       // Gather the row's candidates straight into registers as they land
-      // (each word starts as all ones), then finish in registers.
+      // (each word starts as all ones), then finish in registers.  The
+      // finisher's counters are cleared first, while the candidates land
+      // (after every warp is done with this block's emission).
+      __syncthreads();
+      for (int i = threadIdx.x; i < 3 * kPickBins; i += kThreads) h[i] = 0u;
       unsigned long long* gc = reinterpret_cast<unsigned long long*>(slot_cand);
       unsigned long long e[kRegCand];
 #pragma unroll
@@ -1674,18 +1682,19 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
       uint32_t ok_ = 0u, ak = ~0u, oi = 0u, ai = ~0u;
 #pragma unroll
       for (int j = 0; j < kRegCand; ++j) {
-        const unsigned i = j * kThreads + threadIdx.x;
+        const bool in = j * kThreads + threadIdx.x < cnt;
         ck[j] = (uint32_t)e[j];
         ci[j] = pmax - (uint32_t)(e[j] >> 32);
-        if (i < cnt) {
-          alive |= 1u << j;
-          ok_ |= ck[j]; ak &= ck[j]; oi |= ci[j]; ai &= ci[j];
-        }
+        alive |= (in ? 1u : 0u) << j;
+        ok_ |= in ? ck[j] : 0u;
+        ak &= in ? ck[j] : ~0u;
+        oi |= in ? ci[j] : 0u;
+        ai &= in ? ci[j] : ~0u;
       }
       block_or_and(ok_, ak, oi, ai, ctl);
       if (!ctl->ok) return false;
       finish_in_registers(ck, ci, alive, k_rem, P, ok_, ak, oi, ai, cnt, pmax, h, out_row, k, ctl,
-                          status);
+                          status, true);
     } else if (end == kEndCollect) {
       // Gather the row's candidates as they land (each slot starts as all
       // ones), then finish.
