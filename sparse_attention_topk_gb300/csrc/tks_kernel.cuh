@@ -1542,10 +1542,18 @@ __device__ __forceinline__ bool select_row(const Params& p, int r, int part, uns
     unsigned bin, above;
     const unsigned* suf = h;  // the row's elements above each bin of this round
     int suf_lo = 0;
-    if (kLean && t == 0 && hi - lo <= 32) {
-      // every warp finds the threshold bin and keeps its own suffix sums (in
-      // the unused local candidate area): no block-wide step
-      unsigned* sw = reinterpret_cast<unsigned*>(lcand) + (threadIdx.x >> 5) * 32u;
+    // (the warps' own suffix sums: in the lean kernel's unused local
+    // candidate area; for a whole row on chip, in the slice buffer's tail when
+    // the slice leaves it free)
+    unsigned* sw_base =
+        kLean ? reinterpret_cast<unsigned*>(lcand)
+        : (group == 1 && s.resident && s.nvec * 16 <= kSliceBytes - kWarps * 128)
+            ? reinterpret_cast<unsigned*>(sl + kSliceBytes - kWarps * 128)
+            : nullptr;
+    if (sw_base != nullptr && t == 0 && hi - lo <= 32) {
+      // every warp finds the threshold bin and keeps its own suffix sums: no
+      // block-wide step
+      unsigned* sw = sw_base + (threadIdx.x >> 5) * 32u;
       const Pick pk = warp_window_pick(h, lo, hi, k_rem, sw);
       __syncwarp();
       if (pk.bin == 0xFFFFFFFFu) {
@@ -1766,15 +1774,21 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
   // (its writes to the inputs, the outputs and the workspace included) is
   // complete after it.
   grid_dependency_wait();
-  if (kLean && threadIdx.x == 0) {
-    // the one row's slice copy goes out before anything else
+  // The slice copy of the block's first row goes out before anything else
+  // (the lean kernel's one row; the first row of a block that owns whole rows
+  // in device memory, when it fits on chip).
+  bool first_issued = false;
+  if (threadIdx.x == 0 && (kLean || (p.group == 1 && !p.host_src && !p.cluster))) {
     const int r = blockIdx.x / p.group, part = (int)blockIdx.x - r * p.group;
     bool bad;
     const uint32_t L = r < p.batch ? row_length(p, r, &bad) : 0u;
     if (L > (uint32_t)p.k) {
       const unsigned char* row = p.logits + (int64_t)r * p.row_stride * Elt<DT>::ES;
       const Slice s = slice_geometry<DT>(L, part, p.group, row, p.row_len ? 0u : (uint32_t)p.chunk);
-      issue_slice_copy<DT>(s, row, smem + kSliceOff, ctl, false);
+      if (kLean || s.resident) {
+        issue_slice_copy<DT>(s, row, smem + kSliceOff, ctl, false);
+        first_issued = true;
+      }
     }
   }
   __syncthreads();
@@ -1788,7 +1802,7 @@ __global__ void __launch_bounds__(kThreads, 1) tks_select_kernel(const Params p)
       select_row<DT, kLean>(p, r, (int)blockIdx.x - r * p.group, smem, phase_bits, cl_pending, copy_issued,
                             len_carry);
   } else {
-    bool copy_issued = false;          // the next row's slice copy is in flight
+    bool copy_issued = first_issued;   // this (then the next) row's slice copy is in flight
     uint32_t len_carry = kLenUnknown;  // the next row's length, once loaded
     for (int r = blockIdx.x; r < p.batch; r += gridDim.x)
       if (!select_row<DT, kLean>(p, r, 0, smem, phase_bits, cl_pending, copy_issued, len_carry))
