@@ -400,12 +400,49 @@ class DeviceTiming:
         e1.synchronize()
         return e0.elapsed_time(e1)
 
-    def cold(self, calls=21):
-        """One call after L2 has been flushed by writing twice its size, timed
-        alone (no earlier call to overlap with); median over `calls`."""
+    def cold(self, calls=16, pairs=7):
+        """Latency of one call that follows another kernel with L2 flushed.
+
+        One CUDA graph holds `calls` x [a write of twice the L2 size, one call],
+        another the same writes alone; they are replayed in turn, and the
+        difference over `calls` (median over `pairs` replays of each) is the
+        call's latency after the write kernel, its launch included.  Beside it,
+        `event_us_per_call`: one host-launched call between two CUDA events
+        after the write (median over `calls`), which adds the gap the event
+        record leaves before the launch; event timestamps on this GPU advance
+        in steps of about 1 us, so single calls read on that grid."""
         torch = self.torch
         flush = self.flush
-        cold_us = []
+        g_call, g_flush = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_call, stream=self.stream):
+            for i in range(calls):
+                flush.fill_(float(i))
+                self.call(i)
+        with torch.cuda.graph(g_flush, stream=self.stream):
+            for i in range(calls):
+                flush.fill_(float(i))
+
+        def replay_ms(g):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                torch.cuda._sleep(self.SPIN_CYCLES)
+                e0.record(self.stream)
+                g.replay()
+                e1.record(self.stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
+
+        replay_ms(g_call)  # a graph's first launch uploads it
+        replay_ms(g_flush)
+        diffs = []
+        for _ in range(pairs):
+            a = replay_ms(g_call)
+            b = replay_ms(g_flush)
+            diffs.append((a - b) * 1e3 / calls)
+        del g_call, g_flush
+
+        event_us = []
         for i in range(calls):
             c0 = torch.cuda.Event(enable_timing=True)
             c1 = torch.cuda.Event(enable_timing=True)
@@ -415,12 +452,16 @@ class DeviceTiming:
                 self.call(i)
                 c1.record(self.stream)
             c1.synchronize()
-            cold_us.append(c0.elapsed_time(c1) * 1e3)
+            event_us.append(c0.elapsed_time(c1) * 1e3)
         st = self.tks.device_status(self.stream)
         if st != self.tks.TKS_OK:
             raise RuntimeError(f"device status after the cold calls: {self.tks.status_string(st)}")
-        return {"us_per_call": round(statistics.median(cold_us), 3), "calls": len(cold_us),
-                "flush": f"{2 * self.l2 // 2**20} MiB written before each call"}
+        return {"us_per_call": round(statistics.median(diffs), 3),
+                "spread": [round(min(diffs), 3), round(max(diffs), 3)],
+                "calls": calls, "pairs": pairs,
+                "how": f"graph of {calls} x [{2 * self.l2 // 2**20} MiB write, call] minus graph of "
+                       f"the writes alone, over {calls}; median of {pairs} pairs of replays",
+                "event_us_per_call": round(statistics.median(event_us), 3)}
 
     def release(self):
         self.graphs.clear()
@@ -455,11 +496,13 @@ def other_configs(tks, torch, args, main_name, stream, device, l2, peak, gpu_id)
             if not ok:
                 raise RuntimeError(f"{name}: GPU result differs from the oracle")
             us_call = ms * 1e3 / steps
+            cold = dev.cold()
             gbs = w.algorithmic_bytes / (us_call * 1e-6) / 1e9
             res[name] = {"us_per_row": round(us_call / w.batch, 4), "us_per_call": round(us_call, 3),
                          "batch": w.batch, "n": int(w.row_stride), "k": w.k, "logits": w.dtype,
                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 5), "steps": steps,
-                         "cold_us_per_call": dev.cold(11)["us_per_call"], "matches_oracle": True,
+                         "cold_us_per_call": cold["us_per_call"],
+                         "cold_event_us_per_call": cold["event_us_per_call"], "matches_oracle": True,
                          "plan": dict(zip(("blocks_per_row", "grid"),
                                           tks.plan(w.batch, w.row_stride, w.k, 0 if w.dtype == W.F32 else 1)))}
             dev.release()
@@ -645,7 +688,8 @@ def gpu_arm(args, w, dist, rank, world, device):
                      f"spin kernel ahead of the first event hides the graph's submission",
             "value_is": "back to back: calls queued one after another on one stream, the next "
                         "call's blocks resident while this call finishes (programmatic dependent "
-                        "launch); `cold` is one call alone after an L2 flush",
+                        "launch); `cold` is one call right after a kernel that flushed L2 "
+                        "(graph difference, launch included)",
             "parallelism": f"replicas x{world}",
             "first_round_histogram": "plain shared-memory adds" if args.hist_variant == "plain"
                                      else "warp-aggregated adds (measurement build)",
@@ -663,7 +707,8 @@ def gpu_arm(args, w, dist, rank, world, device):
         },
         "cold": cold,
         "latency": {"back_to_back_us_per_call": round(ms_max * 1e3 / args.steps, 3),
-                    "cold_us_per_call": cold["us_per_call"]},
+                    "cold_us_per_call": cold["us_per_call"],
+                    "cold_event_us_per_call": cold["event_us_per_call"]},
         "gpu_launches": args.steps,
         "e2e": {"value": round(e2e_us_row, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(alg_bytes + (0 if full_rows else 4 * w.batch)),
