@@ -332,11 +332,11 @@ def test_all_equal_rows_and_near_misses(group, dtype):
 
 
 def test_mixed_shapes_back_to_back_on_one_stream():
-    """One stream's workspace serves calls of different shapes queued back to
-    back: row slots are reused with other block counts, other digit-round
-    counts and other candidate counts, and each call cleans up only what the
-    one before it on the slot left.  Every call must still give the oracle's
-    sets."""
+    """One stream's workspace serves calls of different shapes and entry
+    points queued back to back: row slots are reused with other block counts,
+    other digit-round counts and other candidate counts, and each call cleans
+    up only what the one before it on the slot left.  Every call must still
+    give the oracle's sets (rank-ordered calls: the oracle's order)."""
     rng = np.random.Generator(np.random.PCG64(31))
     overflow = W.from_rows("mixed_overflow",
                            [np.full(300000, 0.25, np.float32),
@@ -344,26 +344,39 @@ def test_mixed_shapes_back_to_back_on_one_stream():
     equal = W.from_rows("mixed_equal", [np.full(500000, -3.0, np.float32)], 2048)
     bf16 = W.from_rows("mixed_bf16", [W.f32_to_bf16_bits(rng.standard_normal(200000)) for _ in range(3)],
                        777, W.BF16)
-    cases = [(W.decode_1m_masked(), 0), (W.batch64_ragged(), 0), (overflow, 0), (W.decode_128k(), 0),
-             (equal, 0), (W.batch4_1m_bf16(), 0), (bf16, 5), (W.decode_1m_masked(), 40),
-             (W.decode_4k(), 0), (overflow, 17), (W.decode_1m_masked(), 0)]
+    # (workload, forced blocks per row, entry point)
+    cases = [(W.decode_1m_masked(), 0, "device"), (W.batch64_ragged(), 0, "device"),
+             (overflow, 0, "device"), (W.decode_128k(), 0, "host"), (equal, 0, "device"),
+             (W.batch4_1m_bf16(), 0, "device"), (bf16, 5, "sorted"), (W.decode_1m_masked(), 40, "device"),
+             (W.decode_4k(), 0, "sorted"), (overflow, 17, "device"), (W.decode_1m_masked(), 0, "host"),
+             (W.decode_1m_masked(), 0, "sorted")]
     inputs = {}
-    for w, _ in cases:
-        if w.name not in inputs:
-            rl = torch.from_numpy(w.row_len.copy()).cuda()
-            inputs[w.name] = (_device_values(w), rl)
+    for w, _, entry in cases:
+        key = (w.name, entry == "host")
+        if key not in inputs:
+            if entry == "host":
+                x = torch.from_numpy(w.values.copy()).pin_memory()
+                x = x.view(torch.bfloat16) if w.dtype == W.BF16 else x
+                rl = torch.from_numpy(w.row_len.copy()).pin_memory()
+            else:
+                x = _device_values(w)
+                rl = torch.from_numpy(w.row_len.copy()).cuda()
+            inputs[key] = (x, rl)
     s = torch.cuda.Stream()
     order = [i for _ in range(3) for i in rng.permutation(len(cases))]
     outs = []
     for i in order:
-        w, group = cases[i]
+        w, group, entry = cases[i]
         tks.set_option(tks.TKS_OPT_FORCE_GROUP, group)
-        x, rl = inputs[w.name]
-        outs.append((w, tks.topk_indices(x, w.k, row_len=rl, stream=s)))
+        x, rl = inputs[(w.name, entry == "host")]
+        outs.append((w, entry, tks.topk_indices(x, w.k, row_len=rl, stream=s, sorted=entry == "sorted")))
     tks.set_option(tks.TKS_OPT_FORCE_GROUP, 0)
     assert tks.device_status(s) == tks.TKS_OK
-    for n, (w, o) in enumerate(outs):
+    for n, (w, entry, o) in enumerate(outs):
         try:
-            assert_matches_oracle(w, o.cpu().numpy(), oracle_of(w), check_invariants=False)
+            if entry == "sorted":
+                assert np.array_equal(o.cpu().numpy(), oracle.topk_workload(w, ordered=True))
+            else:
+                assert_matches_oracle(w, o.cpu().numpy(), oracle_of(w), check_invariants=False)
         except AssertionError as e:
-            raise AssertionError(f"call {n} ({w.name}): {e}") from None
+            raise AssertionError(f"call {n} ({w.name}, {entry}): {e}") from None
